@@ -1,0 +1,488 @@
+#!/usr/bin/env python3
+"""Benchmark of the NF4 double-quant hot path on GB300.
+
+One step = one pass of the whole path over the 4096 x 4096 NF4 matrix of the
+4096^2 dequant workload (weights N(0, 0.02) with 0.1% of elements x10 as
+outliers, blocksize 64, s2_blocksize 256):
+    nf4_dequant -> bf16, nf4_dequant -> fp16, nf4_gemv batch 1 (x bf16 N(0,1)).
+Inputs are quantized on the GPU by nf4_quantize (outside the timed region) and
+copied into R rotation sets whose total footprint exceeds 4x the L2, so every
+step reads its weights from HBM. Steps are replayed from CUDA graphs; each
+kernel is bracketed by timing events captured in the graph.
+
+Prints ONE JSON line (rank 0). Usage:
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+For N > 1 run under torch.distributed.run: each rank is an independent replica
+(no data-path collective), value = all ranks' bytes / max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "NF4 dequant GB/s and NF4-GEMV µs/layer, as % of GB300 HBM roofline"
+N_ROWS, K_COLS = 4096, 4096
+BS, S2 = 64, 256
+W_SEED, OUTLIER_SEED, OUTLIER_FRAC = 1, 101, 0.001
+X_SEED = 51                                   # x ~ N(0,1) of the 4096-wide batch-1 GEMV
+WORKLOAD = ("nf4 4096x4096 (N(0,0.02) + 0.1% x10 outliers, blocksize 64, s2 256): "
+            "dequant->bf16 + dequant->fp16 + fused GEMV batch 1 (fp32 accumulate)")
+
+
+def algorithmic_bytes():
+    n = N_ROWS * K_COLS
+    nb = (n + BS - 1) // BS
+    ng = (nb + S2 - 1) // S2
+    quant = n // 2 + nb + 2 * ng + 2 * 256
+    dequant = quant + 2 * n
+    gemv = quant + 2 * K_COLS + 4 * N_ROWS
+    return {"dequant_bf16": dequant, "dequant_fp16": dequant, "gemv_b1": gemv}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(tempfile.gettempdir(), f"nf4_bench_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": sorted(reasons), "samples": 0}
+        sm_sorted = sorted(sm)
+        return {"sm_mhz": sm_sorted[len(sm_sorted) // 2], "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# native arm
+
+def run_native(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    import synth
+    import w4a16_gemv_gb300 as nf4
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    n = N_ROWS * K_COLS
+    bytes_ = algorithmic_bytes()
+    step_bytes = sum(bytes_.values())
+
+    # inputs: synthetic weights quantized on the GPU, x bf16
+    w = torch.from_numpy(synth.weights(W_SEED, n, OUTLIER_FRAC, OUTLIER_SEED)).to(dev)
+    code2 = torch.from_numpy(synth.code2_linear().view(np.float16)).to(dev)
+    q = nf4.nf4_quantize(w, code2, BS, S2)
+    del w
+    x_host = synth.activations(X_SEED, 1, K_COLS)
+    x0 = torch.from_numpy(x_host.view(np.int16)).to(dev).view(torch.bfloat16)
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    set_bytes = (q.packed.numel() + q.absmax_q.numel() + 2 * q.absmax2.numel() + 4 * n + 2 * K_COLS
+                 + 4 * N_ROWS)
+    R = max(2, math.ceil(4 * l2 / set_bytes))
+    sets = []
+    for _ in range(R):
+        sets.append(dict(packed=q.packed.clone(), absmax_q=q.absmax_q.clone(), absmax2=q.absmax2.clone(),
+                         x=x0.clone(), out_bf16=torch.empty(n, dtype=torch.bfloat16, device=dev),
+                         out_fp16=torch.empty(n, dtype=torch.float16, device=dev),
+                         y=torch.empty((1, N_ROWS), dtype=torch.float32, device=dev)))
+    offset = q.offset
+
+    lib = nf4._lib
+    ptr_args = []
+    for s in sets:
+        common = (s["packed"].data_ptr(), s["absmax_q"].data_ptr(), s["absmax2"].data_ptr(),
+                  code2.data_ptr(), offset)
+        ptr_args.append((common, s))
+
+    def step_calls(i, stream_ptr):
+        common, s = ptr_args[i % R]
+        st = lib.nf4_dequant(*common, n, BS, S2, s["out_bf16"].data_ptr(), nf4.NF4_BF16, stream_ptr)
+        st |= lib.nf4_dequant(*common, n, BS, S2, s["out_fp16"].data_ptr(), nf4.NF4_FP16, stream_ptr)
+        st |= lib.nf4_gemv(*common, N_ROWS, K_COLS, BS, S2, s["x"].data_ptr(), 1, s["y"].data_ptr(),
+                           stream_ptr)
+        if st:
+            raise RuntimeError(f"libnf4 call failed with status {st}")
+
+    stream = torch.cuda.Stream(device=dev)
+    sp = stream.cuda_stream
+
+    # graph of S steps with timing events between kernels
+    K, W = args.steps, args.warmup
+    S = max(1, min(K, 7 * R))
+    try:
+        torch.cuda.Event(enable_timing=True, external=True)
+        ext_ok = True
+    except TypeError:
+        ext_ok = False
+
+    def capture(nsteps, with_events):
+        g = torch.cuda.CUDAGraph()
+        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+               for _ in range(nsteps)] if with_events else None
+        with torch.cuda.stream(stream):
+            g.capture_begin()
+            for i in range(nsteps):
+                if evs:
+                    evs[i][0].record(stream)
+                common, s = ptr_args[i % R]
+                lib.nf4_dequant(*common, n, BS, S2, s["out_bf16"].data_ptr(), nf4.NF4_BF16, sp)
+                if evs:
+                    evs[i][1].record(stream)
+                lib.nf4_dequant(*common, n, BS, S2, s["out_fp16"].data_ptr(), nf4.NF4_FP16, sp)
+                if evs:
+                    evs[i][2].record(stream)
+                lib.nf4_gemv(*common, N_ROWS, K_COLS, BS, S2, s["x"].data_ptr(), 1, s["y"].data_ptr(), sp)
+                if evs:
+                    evs[i][3].record(stream)
+            g.capture_end()
+        return g, evs
+
+    # eager sanity pass (also validates every argument once)
+    for i in range(R):
+        step_calls(i, sp)
+    stream.synchronize()
+
+    g_main, evs = capture(S, ext_ok)
+    rem = K % S
+    g_rem = capture(rem, False)[0] if rem else None
+
+    # warm-up: at least W steps
+    done = 0
+    with torch.cuda.stream(stream):
+        while done < W:
+            g_main.replay()
+            done += S
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for _ in range(K // S):
+            g_main.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    elapsed_ms = t0.elapsed_time(t1)
+    clk = clocks.stop()
+
+    # per-kernel durations: every step of the last full replay of the main graph
+    per_kernel = {}
+    names = ["dequant_bf16", "dequant_fp16", "gemv_b1"]
+    if ext_ok and K >= S:
+        for j, name in enumerate(names):
+            ts = [evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(S)]
+            per_kernel[name] = sum(ts) / len(ts) * 1e3   # us
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+
+    # the timed outputs are finite (a cheap guard; parity is the tests' job)
+    assert torch.isfinite(sets[0]["y"]).all().item()
+
+    peak, peak_src = load_peaks()
+    ms_per_step = elapsed_ms / K
+    value = world * step_bytes * K / (elapsed_ms * 1e-3) / 1e9
+
+    detail = {}
+    for name in names:
+        us = per_kernel.get(name)
+        if us:
+            gbs = bytes_[name] / (us * 1e-6) / 1e9
+            d = {"us": round(us, 3), "gbs": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peak, 4)}
+            if name.startswith("gemv"):
+                d["us_per_layer"] = d.pop("us")
+            detail[name] = d
+    dom = "dequant_bf16"
+    roofline = None
+    if dom in per_kernel:
+        ach = bytes_[dom] / (per_kernel[dom] * 1e-6) / 1e9
+        roofline = {"bound": "hbm", "kernel": "nf4_dequant (bf16 out)", "achieved": round(ach, 1),
+                    "peak": peak, "peak_source": peak_src, "unit": "GB/s", "frac": round(ach / peak, 4),
+                    "traffic": read_traffic(dom), "algorithmic_bytes_per_launch": bytes_[dom]}
+
+    e2e = run_e2e(args, dev, q, code2, x_host, bytes_, world) if not args.no_e2e else None
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": round(ms_per_step, 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "bytes_per_step": step_bytes,
+                   "l2_policy": f"rotation over {R} distinct input/output sets "
+                                f"({R * set_bytes / 1e6:.0f} MB > 4x L2 {l2 / 1e6:.0f} MB)",
+                   "timing": f"CUDA graph of {S} steps replayed; events captured between kernels",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": roofline, "detail": detail, "gpu_launches": 3 * K, "clocks": clk, "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu:
+        result["cpu_baseline"] = cpu_baseline(args, q, x_host, bytes_)
+    return result
+
+
+def read_traffic(kernel_name):
+    """DRAM bytes per launch from the committed ncu summary, if it still
+    matches the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        import hashlib
+        src = os.path.join(ROOT, "w4a16_gemv_gb300", "csrc", t["source"])
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        if h != t["source_sha256"]:
+            return None
+        return t["kernels"][kernel_name]["dram_bytes_per_launch"]
+    except Exception:
+        return None
+
+
+def run_e2e(args, dev, q, code2, x_host, bytes_, world):
+    """Same step through the public API with host buffers: H2D of the step's
+    inputs from pinned memory and D2H of its outputs inside the timed region."""
+    import numpy as np
+    import torch
+
+    import w4a16_gemv_gb300 as nf4
+    n = N_ROWS * K_COLS
+    h_packed = q.packed.cpu().pin_memory()
+    h_absmax_q = q.absmax_q.cpu().pin_memory()
+    h_absmax2 = q.absmax2.cpu().pin_memory()
+    h_code2 = code2.cpu().pin_memory()
+    h_x = torch.from_numpy(x_host.view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_bf16 = torch.empty(n, dtype=torch.bfloat16).pin_memory()
+    h_fp16 = torch.empty(n, dtype=torch.float16).pin_memory()
+    h_y = torch.empty((1, N_ROWS), dtype=torch.float32).pin_memory()
+    d = dict(packed=torch.empty_like(q.packed), absmax_q=torch.empty_like(q.absmax_q),
+             absmax2=torch.empty_like(q.absmax2), code2=torch.empty_like(code2),
+             x=torch.empty((1, K_COLS), dtype=torch.bfloat16, device=dev),
+             bf16=torch.empty(n, dtype=torch.bfloat16, device=dev),
+             fp16=torch.empty(n, dtype=torch.float16, device=dev),
+             y=torch.empty((1, N_ROWS), dtype=torch.float32, device=dev))
+    h2d = sum(t.numel() * t.element_size() for t in (h_packed, h_absmax_q, h_absmax2, h_code2, h_x))
+    d2h = sum(t.numel() * t.element_size() for t in (h_bf16, h_fp16, h_y))
+
+    def step():
+        for k, h in (("packed", h_packed), ("absmax_q", h_absmax_q), ("absmax2", h_absmax2),
+                     ("code2", h_code2), ("x", h_x)):
+            d[k].copy_(h, non_blocking=True)
+        nf4.nf4_dequant(d["packed"], d["absmax_q"], d["absmax2"], d["code2"], q.offset, n, BS, S2,
+                        out=d["bf16"], out_dtype=torch.bfloat16)
+        nf4.nf4_dequant(d["packed"], d["absmax_q"], d["absmax2"], d["code2"], q.offset, n, BS, S2,
+                        out=d["fp16"], out_dtype=torch.float16)
+        nf4.nf4_gemv(d["packed"], d["absmax_q"], d["absmax2"], d["code2"], q.offset, N_ROWS, K_COLS,
+                     d["x"], y=d["y"], blocksize=BS, s2_blocksize=S2)
+        h_bf16.copy_(d["bf16"], non_blocking=True)
+        h_fp16.copy_(d["fp16"], non_blocking=True)
+        h_y.copy_(d["y"], non_blocking=True)
+
+    steps = max(3, min(args.steps, 50))
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    step_bytes = sum(bytes_.values())
+    return {"value": round(world * step_bytes * steps / dt / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "ms_per_step": round(dt / steps * 1e3, 4)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline and reference arm)
+
+def _oracle_inputs(q=None, x_host=None):
+    import numpy as np
+
+    import oracle
+    import synth
+    n = N_ROWS * K_COLS
+    if q is not None:
+        t = oracle.NF4Tensor(q.packed.cpu().numpy(), q.absmax_q.cpu().numpy(),
+                             q.absmax2.cpu().numpy().view(np.uint16), synth.code2_linear(), q.offset, n,
+                             BS, S2)
+    else:
+        w = synth.weights(W_SEED, n, OUTLIER_FRAC, OUTLIER_SEED)
+        t = oracle.quantize(w, BS, S2, synth.code2_linear())
+    if x_host is None:
+        x_host = synth.activations(X_SEED, 1, K_COLS)
+    return t, x_host
+
+
+def _oracle_step(t, x_host, rows):
+    """One bounded sample of the step: the first `rows` rows of the matrix."""
+    import oracle
+    sub = oracle.NF4Tensor(t.packed, t.absmax_q, t.absmax2, t.code2, t.offset, rows * K_COLS, BS, S2)
+    oracle.dequant(sub, oracle.BF16)
+    oracle.dequant(sub, oracle.FP16)
+    oracle.gemv(sub, rows, K_COLS, x_host)
+
+
+def _sample_rows(t, x_host, budget_s):
+    t0 = time.perf_counter()
+    _oracle_step(t, x_host, 8)
+    per_row = (time.perf_counter() - t0) / 8
+    return max(1, min(N_ROWS, int(budget_s / per_row)))
+
+
+def cpu_baseline(args, q, x_host, bytes_):
+    t, x_host = _oracle_inputs(q, x_host)
+    rows = _sample_rows(t, x_host, 2.0)
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        _oracle_step(t, x_host, rows)
+        reps += 1
+        if time.perf_counter() - t0 > 10.0:
+            break
+    dt = time.perf_counter() - t0
+    frac = rows / N_ROWS
+    v = sum(bytes_.values()) * frac * reps / dt / 1e9
+    return {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {rows} of {N_ROWS} rows per step (dequant bf16 + fp16 + fp64 GEMV), "
+                      f"{reps} steps in {dt:.1f} s, single-threaded C oracle"}
+
+
+def run_reference(args):
+    bytes_ = algorithmic_bytes()
+    t, x_host = _oracle_inputs()
+    K, W = args.steps, args.warmup
+    budget = max(0.002, 60.0 / max(1, K + W))
+    rows = _sample_rows(t, x_host, budget)
+    for _ in range(W):
+        _oracle_step(t, x_host, rows)
+    t0 = time.perf_counter()
+    for _ in range(K):
+        _oracle_step(t, x_host, rows)
+    dt = time.perf_counter() - t0
+    frac = rows / N_ROWS
+    step_bytes = sum(bytes_.values()) * frac
+    v = step_bytes * K / dt / 1e9
+    sample = (f"first {rows} of {N_ROWS} rows per step (dequant bf16 + fp16 + fp64 GEMV), "
+              f"single-threaded C oracle")
+    return {"metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": args.gpus, "steps": K,
+            "warmup": W, "ms_per_step": round(dt / K * 1e3, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "impl": "reference", "config": {"workload": WORKLOAD, "parallelism": "single CPU core"},
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50000)
+    ap.add_argument("--warmup", type=int, default=500)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.steps < 1:
+        raise SystemExit("--steps must be >= 1")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        result = run_native(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+if __name__ == "__main__":
+    main()

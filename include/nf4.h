@@ -1,0 +1,185 @@
+/*
+ * nf4.h -- C ABI of libnf4: NF4 (4-bit NormalFloat) weights with double
+ * quantization on NVIDIA GB300 (sm_103a).
+ *
+ * Format (the bitsandbytes-style layout described by the pages):
+ *   - Code book: the sixteen NF4 values printed in "NF4反量化算子优化"
+ *     (roundaboutt.github.io), section "NF4 table".
+ *   - A tensor of n elements is flattened and cut into blocks of `blocksize`
+ *     consecutive elements; blocks are grouped by `s2_blocksize`
+ *     ("NF4 双重量化反量化 CUDA Kernel 实现报告", section 1.2).
+ *   - packed   : uint8 [ceil(n/2)], two 4-bit code indices per byte; element
+ *                2t is the HIGH nibble of byte t, element 2t+1 the LOW nibble
+ *                (same report, section 2.2). For odd n the last low nibble is
+ *                padding.
+ *   - absmax_q : uint8 [ceil(n/blocksize)], index into code2 per block.
+ *   - absmax2  : binary16 bit patterns [ceil(nblocks/s2_blocksize)], one
+ *                second-level scale per group.
+ *   - code2    : binary16 bit patterns [256], second-level code table.
+ *   - offset   : binary32 scalar added to every decoded block scale.
+ *   Dequantization (same report, section 1.3), for element k:
+ *     b = k / blocksize, g = b / s2_blocksize,
+ *     s = fp32( fp32(code2[absmax_q[b]] * absmax2[g]) + offset ),
+ *     out[k] = round16( fp32( NF4[idx(k)] * s ) ),
+ *   every operation a separately rounded binary32 operation (no fused
+ *   multiply-add), round16 = round-to-nearest-even into bfloat16 or binary16
+ *   (subnormals kept).
+ *
+ * Conventions for every entry point:
+ *   - All array arguments are DEVICE pointers owned by the caller; the library
+ *     never allocates, frees or keeps them, and keeps no global state beyond
+ *     a per-device cache of the SM count.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and the call returns without synchronising.
+ *   - Argument checks run on the host before any launch; on failure nothing
+ *     is enqueued and an error status is returned. A launch failure returns
+ *     NF4_ERR_CUDA (the CUDA error is consumed; nf4_last_cuda_error() returns
+ *     it). Kernels never trap.
+ *   - Sizes are element counts (int64). Misaligned vector pointers are not an
+ *     error: such calls run a slower kernel. Pointers not aligned to their
+ *     element size are NF4_ERR_MISALIGNED.
+ */
+#ifndef NF4_H_
+#define NF4_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define NF4_API __attribute__((visibility("default")))
+#else
+#define NF4_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st* nf4_stream_t;
+
+typedef enum {
+  NF4_OK = 0,
+  NF4_ERR_NULL = 1,                  /* a required pointer is NULL */
+  NF4_ERR_INVALID_SIZE = 2,          /* negative size, odd K, size overflow */
+  NF4_ERR_UNSUPPORTED_BLOCKSIZE = 3, /* blocksize / s2_blocksize not a supported power of two */
+  NF4_ERR_MISALIGNED = 4,            /* pointer not aligned to its element size */
+  NF4_ERR_UNSUPPORTED_DTYPE = 5,     /* out_dtype not NF4_BF16 / NF4_FP16 */
+  NF4_ERR_UNSUPPORTED_BATCH = 6,     /* GEMV batch outside 1..8 */
+  NF4_ERR_CUDA = 7,                  /* a CUDA runtime call failed */
+  NF4_ERR_WORKSPACE = 8              /* workspace missing or too small */
+} nf4_status;
+
+typedef enum { NF4_BF16 = 0, NF4_FP16 = 1 } nf4_dtype;
+
+/* Library version as major*10000 + minor*100 + patch. */
+NF4_API int nf4_version(void);
+
+/* Static, human-readable name of a status code (never NULL). */
+NF4_API const char* nf4_status_string(nf4_status status);
+
+/* The cudaError_t value behind the last NF4_ERR_CUDA returned on this host
+ * thread (0 if none). */
+NF4_API int nf4_last_cuda_error(void);
+
+/*
+ * nf4_dequant -- expand n NF4 elements to bfloat16 or binary16.
+ * Defined by "NF4 双重量化反量化 CUDA Kernel 实现报告", section 1.3 (formula)
+ * and section 2.2 (nibble order); see the format notes above.
+ *
+ *   packed       uint8  [ceil(n/2)]
+ *   absmax_q     uint8  [ceil(n/blocksize)]
+ *   absmax2      uint16 [ceil(ceil(n/blocksize)/s2_blocksize)]  (binary16 bits)
+ *   code2        uint16 [256]                                   (binary16 bits)
+ *   offset       binary32 scalar (by value)
+ *   n            number of elements, >= 0 (0 enqueues nothing and returns NF4_OK)
+ *   blocksize    power of two, 2 .. 2^20 (64 is the usual value)
+ *   s2_blocksize power of two, 1 .. 2^20 (256 is the usual value)
+ *   out          [n] 16-bit elements of out_dtype, 2-byte aligned; written
+ *                bit-exactly per the formula. Fastest when out is 16-byte
+ *                and packed 4-byte aligned.
+ *   out_dtype    NF4_BF16 or NF4_FP16
+ * Errors: NF4_ERR_NULL, NF4_ERR_INVALID_SIZE (n < 0 or n > 2^40),
+ *   NF4_ERR_UNSUPPORTED_BLOCKSIZE, NF4_ERR_MISALIGNED (absmax2, code2, out not
+ *   2-byte aligned), NF4_ERR_UNSUPPORTED_DTYPE, NF4_ERR_CUDA.
+ */
+NF4_API nf4_status nf4_dequant(const uint8_t* packed, const uint8_t* absmax_q,
+                       const uint16_t* absmax2, const uint16_t* code2, float offset,
+                       int64_t n, int32_t blocksize, int32_t s2_blocksize, void* out,
+                       nf4_dtype out_dtype, nf4_stream_t stream);
+
+/*
+ * nf4_gemv -- decode GEMV with the dequantization fused: y = W_hat x.
+ * The fused form follows "RTX 4060 上的 LLM 量化实测：4-bit decode 比 FP16
+ * 慢在哪里", section "Fused kernel：把反量化搬到片上" (unpack, look up, scale
+ * and accumulate on chip in fp32; only y is written); the per-warp row
+ * structure follows "CUDA 进阶手册 / 量化与 GEMV", section "GEMV kernel 的写法".
+ *
+ *   packed, absmax_q, absmax2, code2, offset, blocksize, s2_blocksize:
+ *                the quantized N x K weight, row-major with K contiguous,
+ *                quantized as one flattened tensor of N*K elements
+ *                (element (r, k) is flat index r*K + k).
+ *   N, K         output and input features; N >= 0, K >= 0 and even.
+ *   x            bfloat16 bit patterns [batch][K], 2-byte aligned.
+ *   batch        1 .. 8 activation vectors.
+ *   y            binary32 [batch][N], 4-byte aligned:
+ *                y[b][r] = sum_k W_hat[r][k] * x[b][k], with W_hat[r][k] the
+ *                binary32 dequantized weight (before 16-bit rounding) and
+ *                binary32 accumulation in an unspecified order. The result
+ *                satisfies |y - y_exact| <= 1e-3 * sum_k |W_hat x| + 1e-6.
+ *                K == 0 writes zeros.
+ * Errors: NF4_ERR_NULL, NF4_ERR_INVALID_SIZE (N < 0, K < 0, K odd, N*K > 2^40),
+ *   NF4_ERR_UNSUPPORTED_BLOCKSIZE, NF4_ERR_MISALIGNED,
+ *   NF4_ERR_UNSUPPORTED_BATCH, NF4_ERR_CUDA.
+ */
+NF4_API nf4_status nf4_gemv(const uint8_t* packed, const uint8_t* absmax_q,
+                    const uint16_t* absmax2, const uint16_t* code2, float offset,
+                    int64_t N, int64_t K, int32_t blocksize, int32_t s2_blocksize,
+                    const uint16_t* x, int32_t batch, float* y, nf4_stream_t stream);
+
+/*
+ * nf4_quantize_workspace_size -- bytes of device workspace nf4_quantize needs
+ * for n elements (0 for n <= 0 or unsupported block sizes).
+ */
+NF4_API size_t nf4_quantize_workspace_size(int64_t n, int32_t blocksize, int32_t s2_blocksize);
+
+/*
+ * nf4_quantize -- NF4 quantization with double quantization of a binary32
+ * tensor, the encoding that nf4_dequant inverts.
+ * First level: "NF4反量化算子优化", section "双量化 / 第一层量化" (flatten,
+ * blocks of `blocksize`, per-block absmax, divide, nearest code, two codes per
+ * byte). Second level: the same section "第二层量化" and
+ * "NF4 双重量化反量化 CUDA Kernel 实现报告", section 1.2 (absmax quantized to
+ * uint8 indices into code2, one binary16 absmax2 per group, a binary32 offset).
+ * Where the pages leave a step open this library fixes it as follows:
+ *   absmax[b]   = max |w| over the elements of block b present;
+ *   v           = w / absmax[b] (binary32 division; 0 if absmax[b] == 0);
+ *   code index  = argmin_j |v - NF4[j]| in binary64, ties to the lower j;
+ *   offset      = binary32( S / nblocks ), S the binary64 sum of absmax taken
+ *                 group by group (blocks in order within a group, then the
+ *                 group sums in order);
+ *   absmax2[g]  = binary16 RNE of max |absmax[b] - offset| (binary32) over the
+ *                 blocks of group g;
+ *   absmax_q[b] = argmin_i |r - code2[i]| in binary64, ties to the lower i,
+ *                 r = binary32 (absmax[b] - offset) / absmax2[g] (0 if absmax2 is 0).
+ *
+ *   w            binary32 [n], finite values, 4-byte aligned
+ *   n, blocksize, s2_blocksize: as for nf4_dequant
+ *   code2        binary16 bits [256], increasing (caller-chosen table)
+ *   packed, absmax_q, absmax2: outputs, sized as for nf4_dequant
+ *   offset       device pointer to ONE binary32 output
+ *   workspace    device scratch of at least nf4_quantize_workspace_size() bytes,
+ *                8-byte aligned; contents on entry are ignored
+ * Errors: NF4_ERR_NULL, NF4_ERR_INVALID_SIZE, NF4_ERR_UNSUPPORTED_BLOCKSIZE,
+ *   NF4_ERR_MISALIGNED, NF4_ERR_WORKSPACE, NF4_ERR_CUDA.
+ */
+NF4_API nf4_status nf4_quantize(const float* w, int64_t n, int32_t blocksize, int32_t s2_blocksize,
+                        const uint16_t* code2, uint8_t* packed, uint8_t* absmax_q,
+                        uint16_t* absmax2, float* offset, void* workspace,
+                        size_t workspace_bytes, nf4_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NF4_H_ */

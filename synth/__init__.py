@@ -5,61 +5,78 @@ quantization, dequantization or GEMV arithmetic.  Both the CPU oracle and the
 CUDA path consume what it produces, so it is the only code they share.
 
 Generator: SplitMix64 (G. Steele, D. Lea, C. Flood, "Fast splittable
-pseudorandom number generators", OOPSLA 2014) used counter-style: the i-th
-64-bit draw of stream ``key`` is ``mix(key * 2**32 + i)`` through the
-SplitMix64 output function, so any slice regenerates independently.  Normal
-deviates come from the Box-Muller transform of two 53-bit uniforms in (0, 1].
+pseudorandom number generators", OOPSLA 2014) used counter-style: draw i of
+stream ``key`` is the SplitMix64 output mix of ``key * 2**32 + (i + 1) *
+0x9E3779B97F4A7C15`` (mod 2**64), so any slice regenerates independently.
+Normal deviates come from the Box-Muller transform of two 53-bit uniforms in
+(0, 1].  The core is ``synth.c`` (threaded C, loaded with ctypes).
 """
 from __future__ import annotations
 
-from dataclasses import dataclass, field
+import ctypes
+import os
+import subprocess
+from dataclasses import dataclass
 
 import numpy as np
 
-_GOLDEN = np.uint64(0x9E3779B97F4A7C15)
-_M1 = np.uint64(0xBF58476D1CE4E5B9)
-_M2 = np.uint64(0x94D049BB133111EB)
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "synth.c")
+_LIB_PATH = os.path.join(_HERE, "_synth.so")
+_lib = None
 
 
-def _mix(z: np.ndarray) -> np.ndarray:
-    z = z.copy()
-    z ^= z >> np.uint64(30)
-    z *= _M1
-    z ^= z >> np.uint64(27)
-    z *= _M2
-    z ^= z >> np.uint64(31)
-    return z
+def build(force: bool = False) -> str:
+    """Compile the generator core (C, pthreads)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+                        "-shared", "-pthread", _SRC, "-o", tmp, "-lm"], check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        P, I64, U64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64
+        lib.synth_normal_f32.argtypes = [U64, I64, I64, ctypes.c_double, P, ctypes.c_int]
+        lib.synth_normal_bf16.argtypes = [U64, I64, I64, P, ctypes.c_int]
+        lib.synth_draws.argtypes = [U64, I64, I64, P, ctypes.c_int]
+        _lib = lib
+    return _lib
+
+
+def _threads() -> int:
+    try:
+        return max(1, min(32, len(os.sched_getaffinity(0))))
+    except AttributeError:  # pragma: no cover
+        return max(1, min(32, os.cpu_count() or 1))
 
 
 def draws(key: int, start: int, count: int) -> np.ndarray:
     """uint64 draws [start, start+count) of stream ``key`` (SplitMix64 sequence)."""
-    base = np.uint64((key * (1 << 32)) & 0xFFFFFFFFFFFFFFFF)
-    ctr = np.arange(start + 1, start + count + 1, dtype=np.uint64)
-    with np.errstate(over="ignore"):
-        return _mix(base + ctr * _GOLDEN)
+    out = np.empty(count, np.uint64)
+    if count:
+        _load().synth_draws(key, start, count, out.ctypes.data, _threads())
+    return out
 
 
-def uniform(key: int, start: int, count: int) -> np.ndarray:
-    """float64 uniforms in (0, 1] from the top 53 bits of each draw."""
-    d = draws(key, start, count)
-    return ((d >> np.uint64(11)).astype(np.float64) + 1.0) * (2.0 ** -53)
-
-
-def normal(key: int, n: int, std: float = 1.0, chunk: int = 1 << 24) -> np.ndarray:
+def normal(key: int, n: int, std: float = 1.0, start: int = 0) -> np.ndarray:
     """float32 N(0, std^2): element 2p and 2p+1 from uniforms 2p, 2p+1 (Box-Muller)."""
     out = np.empty(n, np.float32)
-    npairs = (n + 1) // 2
-    for p0 in range(0, npairs, chunk):
-        p1 = min(npairs, p0 + chunk)
-        u = uniform(key, 2 * p0, 2 * (p1 - p0))
-        u1, u2 = u[0::2], u[1::2]
-        r = np.sqrt(-2.0 * np.log(u1)) * std
-        t = 2.0 * np.pi * u2
-        z = np.empty(2 * (p1 - p0), np.float64)
-        z[0::2] = r * np.cos(t)
-        z[1::2] = r * np.sin(t)
-        e0, e1 = 2 * p0, min(n, 2 * p1)
-        out[e0:e1] = z[: e1 - e0].astype(np.float32)
+    if n:
+        _load().synth_normal_f32(key, start, n, float(std), out.ctypes.data, _threads())
+    return out
+
+
+def normal_bf16(key: int, n: int) -> np.ndarray:
+    """N(0, 1) rounded to bfloat16 (nearest even), as uint16 bit patterns."""
+    out = np.empty(n, np.uint16)
+    if n:
+        _load().synth_normal_bf16(key, 0, n, out.ctypes.data, _threads())
     return out
 
 
@@ -72,13 +89,10 @@ def distinct_indices(key: int, n: int, m: int) -> np.ndarray:
     return np.sort(idx.astype(np.int64))
 
 
-def to_bf16_bits(a: np.ndarray) -> np.ndarray:
-    """float32 -> bfloat16 bit patterns, round to nearest even (finite inputs).
-
-    Used only to shape the bf16 activation input x."""
-    u = np.ascontiguousarray(a, np.float32).view(np.uint32).astype(np.uint64)
-    lsb = (u >> np.uint64(16)) & np.uint64(1)
-    return ((u + np.uint64(0x7FFF) + lsb) >> np.uint64(16)).astype(np.uint16)
+def code2_linear() -> np.ndarray:
+    """The workloads' second-level table: binary16 of (i - 127.5) / 127.5, i < 256
+    (binary64 value rounded once to binary16), as uint16 bit patterns."""
+    return ((np.arange(256, dtype=np.float64) - 127.5) / 127.5).astype(np.float16).view(np.uint16)
 
 
 # --------------------------------------------------------------------------
@@ -101,7 +115,7 @@ def weights(seed: int, n: int, outlier_frac: float = 0.0, outlier_seed: int | No
 
 def activations(seed: int, batch: int, K: int) -> np.ndarray:
     """x ~ N(0, 1), rounded to bf16, as uint16 bit patterns [batch, K]."""
-    return to_bf16_bits(normal(seed, batch * K, 1.0)).reshape(batch, K)
+    return normal_bf16(seed, batch * K).reshape(batch, K)
 
 
 @dataclass(frozen=True)

@@ -1,0 +1,117 @@
+"""The C ABI without a GPU: the library loads, exports every symbol that
+include/nf4.h declares, and rejects bad arguments on the host before any CUDA
+call (so these calls are safe on a machine without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nf4.h")
+
+OK, ERR_NULL, ERR_SIZE, ERR_BS, ERR_ALIGN, ERR_DTYPE, ERR_BATCH, ERR_CUDA, ERR_WS = range(9)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__._build_module().build()
+    import w4a16_gemv_gb300 as nf4
+    return nf4._lib
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"NF4_API\s+[\w\s\*]+?\b(nf4_\w+)\s*\(", text)
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert set(names) == {"nf4_version", "nf4_status_string", "nf4_last_cuda_error", "nf4_dequant",
+                          "nf4_gemv", "nf4_quantize_workspace_size", "nf4_quantize"}
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_version(lib):
+    text = open(HEADER).read()
+    codes = dict((m.group(1), int(m.group(2))) for m in re.finditer(r"(NF4_(?:OK|ERR_\w+))\s*=\s*(\d+)", text))
+    assert codes["NF4_OK"] == 0 and len(codes) == 9
+    for name, v in codes.items():
+        s = lib.nf4_status_string(v).decode()
+        assert s.startswith(name), (name, s)
+    assert lib.nf4_status_string(99).decode().startswith("NF4: unknown")
+    assert lib.nf4_version() == 100
+    assert lib.nf4_last_cuda_error() == 0
+
+
+A = 0x100000  # a fake, well-aligned address: never dereferenced by these calls
+P = ctypes.c_void_p
+
+
+def dq(lib, n=128, packed=A, absmax_q=A, absmax2=A, code2=A, out=A, bs=64, s2=256, dtype=0):
+    return lib.nf4_dequant(P(packed), P(absmax_q), P(absmax2), P(code2), 0.5, n, bs, s2, P(out),
+                           dtype, None)
+
+
+def gv(lib, N=16, K=64, x=A, y=A, batch=1, bs=64, s2=256, packed=A):
+    return lib.nf4_gemv(P(packed), P(A), P(A), P(A), 0.0, N, K, bs, s2, P(x), batch, P(y), None)
+
+
+def test_dequant_argument_errors(lib):
+    assert dq(lib, n=-1) == ERR_SIZE
+    assert dq(lib, n=(1 << 40) + 1) == ERR_SIZE
+    for bs in (0, 1, 3, 48, 65, 1 << 21, -64):
+        assert dq(lib, bs=bs) == ERR_BS, bs
+    for s2 in (0, 3, 255, 1 << 21):
+        assert dq(lib, s2=s2) == ERR_BS, s2
+    assert dq(lib, dtype=2) == ERR_DTYPE
+    assert dq(lib, dtype=-1) == ERR_DTYPE
+    assert dq(lib, n=0, packed=0, absmax_q=0, absmax2=0, code2=0, out=0) == OK
+    assert dq(lib, packed=0) == ERR_NULL
+    assert dq(lib, absmax_q=0) == ERR_NULL
+    assert dq(lib, absmax2=0) == ERR_NULL
+    assert dq(lib, code2=0) == ERR_NULL
+    assert dq(lib, out=0) == ERR_NULL
+    assert dq(lib, out=A + 1) == ERR_ALIGN
+    assert dq(lib, absmax2=A + 1) == ERR_ALIGN
+    assert dq(lib, code2=A + 3) == ERR_ALIGN
+
+
+def test_gemv_argument_errors(lib):
+    assert gv(lib, N=-1) == ERR_SIZE
+    assert gv(lib, K=-2) == ERR_SIZE
+    assert gv(lib, K=63) == ERR_SIZE
+    assert gv(lib, N=1 << 30, K=1 << 12) == ERR_SIZE
+    assert gv(lib, bs=96) == ERR_BS
+    for b in (0, 9, -1):
+        assert gv(lib, batch=b) == ERR_BATCH, b
+    assert gv(lib, N=0, y=0, x=0) == OK
+    assert gv(lib, y=0) == ERR_NULL
+    assert gv(lib, x=0) == ERR_NULL
+    assert gv(lib, packed=0) == ERR_NULL
+    assert gv(lib, y=A + 2) == ERR_ALIGN
+    assert gv(lib, x=A + 1) == ERR_ALIGN
+
+
+def test_quantize_argument_errors_and_workspace_size(lib):
+    lib.nf4_quantize_workspace_size.restype = ctypes.c_size_t
+    ws = lib.nf4_quantize_workspace_size
+    assert ws(0, 64, 256) == 0 and ws(-5, 64, 256) == 0 and ws(100, 63, 256) == 0
+    # n = 64*256*3 + 1: 769 blocks (256-aligned float array) + 4 groups of binary64
+    assert ws(64 * 256 * 3 + 1, 64, 256) == 3328 + 4 * 8
+    assert ws(1 << 20, 64, 256) == 16384 * 4 + 64 * 8
+
+    def q(n=1000, w=A, ws_ptr=A, ws_bytes=1 << 20, off=A, bs=64):
+        return lib.nf4_quantize(P(w), n, bs, 256, P(A), P(A), P(A), P(A), P(off), P(ws_ptr),
+                                ctypes.c_size_t(ws_bytes), None)
+    assert q(n=-1) == ERR_SIZE
+    assert q(bs=5) == ERR_BS
+    assert q(n=0, w=0) == OK
+    assert q(w=0) == ERR_NULL
+    assert q(off=0) == ERR_NULL
+    assert q(w=A + 2) == ERR_ALIGN
+    assert q(ws_ptr=0) == ERR_WS
+    assert q(ws_bytes=16) == ERR_WS
+    assert q(ws_ptr=A + 4) == ERR_WS

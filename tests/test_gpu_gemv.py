@@ -1,0 +1,113 @@
+"""GPU parity for nf4_gemv: |y - y_ref| <= 1e-3 * sum|w_hat x| + 1e-6 against
+the oracle's binary64 GEMV."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_helpers import assert_gemv_close, gpu_gemv, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def _layer(layer):
+    w = synth.weights(layer.seed, layer.N * layer.K)
+    return oracle.quantize(w, 64, 256, synth.code2_linear())
+
+
+@pytest.mark.parametrize("layer", synth.QWEN_1P5B_LAYERS, ids=lambda l: l.name)
+def test_config2_qwen_layers_batch1(layer):
+    t = _layer(layer)
+    x = synth.activations(synth.QWEN_X_SEED, 1, layer.K)
+    y = gpu_gemv(t, layer.N, layer.K, x)
+    y_ref, s_abs = oracle.gemv(t, layer.N, layer.K, x)
+    assert_gemv_close(y, y_ref, s_abs, layer.name)
+
+
+@pytest.mark.parametrize("layer", synth.LLAMA_7B_LAYERS, ids=lambda l: l.name)
+def test_config3_llama7b_layers(layer):
+    t = _layer(layer)
+    d = to_device(t)
+    for batch in synth.LLAMA_BATCHES:
+        x = synth.activations(synth.llama_x_seed(batch), batch, layer.K)
+        y = gpu_gemv(t, layer.N, layer.K, x, d=d)
+        y_ref, s_abs = oracle.gemv(t, layer.N, layer.K, x)
+        assert_gemv_close(y, y_ref, s_abs, f"{layer.name} batch {batch}")
+
+
+@pytest.mark.parametrize("K", [1536, 4096, 1032, 1040, 4104, 70, 2, 8960])
+@pytest.mark.parametrize("batch", [1, 2, 3, 4, 5, 6, 7, 8])
+def test_all_batches_and_chunk_widths(K, batch):
+    """Every batch size with K values that select each chunk width (16, 8, 4
+    packed bytes per lane) and the generic kernel (K % 8 != 0)."""
+    N = 37
+    w = synth.weights(500 + K, N * K, 0.001, 501)
+    t = oracle.quantize(w, 64, 256, synth.code2_linear())
+    x = synth.activations(600 + batch, batch, K)
+    y = gpu_gemv(t, N, K, x)
+    y_ref, s_abs = oracle.gemv(t, N, K, x)
+    assert_gemv_close(y, y_ref, s_abs, f"N={N} K={K} batch={batch}")
+
+
+@pytest.mark.parametrize("N", [1, 2, 7, 31, 32, 33, 255, 256, 257, 1000])
+def test_row_counts(N):
+    K = 1536
+    w = synth.weights(700 + N, N * K)
+    t = oracle.quantize(w, 64, 256, synth.code2_linear())
+    for batch in (1, 4):
+        x = synth.activations(800 + N, batch, K)
+        y = gpu_gemv(t, N, K, x)
+        y_ref, s_abs = oracle.gemv(t, N, K, x)
+        assert_gemv_close(y, y_ref, s_abs, f"N={N} batch={batch}")
+
+
+@pytest.mark.parametrize("bs,s2", [(32, 256), (128, 4), (16, 256), (8, 1), (2, 1), (4096, 1)])
+def test_block_sizes(bs, s2):
+    N, K = 40, 4096
+    w = synth.weights(900 + bs, N * K, 0.001, 901)
+    t = oracle.quantize(w, bs, s2, synth.code2_linear())
+    for batch in (1, 3):
+        x = synth.activations(902, batch, K)
+        y = gpu_gemv(t, N, K, x)
+        y_ref, s_abs = oracle.gemv(t, N, K, x)
+        assert_gemv_close(y, y_ref, s_abs, f"bs={bs} s2={s2} batch={batch}")
+
+
+def test_ragged_k_blocks_straddle_rows():
+    """K = 1000 is not a multiple of 64: blocks straddle rows (generic kernel)."""
+    N, K = 33, 1000
+    w = synth.weights(950, N * K)
+    t = oracle.quantize(w, 64, 256, synth.code2_linear())
+    x = synth.activations(951, 2, K)
+    y = gpu_gemv(t, N, K, x)
+    y_ref, s_abs = oracle.gemv(t, N, K, x)
+    assert_gemv_close(y, y_ref, s_abs)
+
+
+def test_misaligned_x_and_zero_k():
+    N, K = 64, 1536
+    w = synth.weights(960, N * K)
+    t = oracle.quantize(w, 64, 256, synth.code2_linear())
+    x = synth.activations(961, 1, K)
+    y = gpu_gemv(t, N, K, x, x_offset=1)
+    y_ref, s_abs = oracle.gemv(t, N, K, x)
+    assert_gemv_close(y, y_ref, s_abs, "misaligned x")
+    y0 = gpu_gemv(t, N, 0, np.zeros((2, 0), np.uint16))
+    assert np.all(y0 == 0.0)
+
+
+def test_special_inputs():
+    """x = 0 gives y = 0; a one-hot x gives the dequantized column."""
+    N, K = 128, 4096
+    w = synth.weights(970, N * K)
+    t = oracle.quantize(w, 64, 256, synth.code2_linear())
+    y = gpu_gemv(t, N, K, np.zeros((1, K), np.uint16))
+    assert np.all(y == 0.0)
+    W = oracle.dequant_f32(t).reshape(N, K).astype(np.float64)
+    x = np.zeros((3, K), np.uint16)
+    cols = [0, 1, 4095]
+    for b, c in enumerate(cols):
+        x[b, c] = 0x3F80                           # bf16 1.0
+    y = gpu_gemv(t, N, K, x)
+    for b, c in enumerate(cols):
+        np.testing.assert_allclose(y[b], W[:, c], rtol=1e-3, atol=1e-6)

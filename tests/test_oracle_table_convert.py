@@ -138,3 +138,8 @@ def test_code2_linear_table():
     # each entry is within half an fp16 ulp of the exact value
     half_ulp = np.array([2.0 ** (math.floor(math.log2(abs(v))) - 11) for v in exact])
     assert np.all(np.abs(vals - exact) <= half_ulp)
+
+
+def test_generator_code2_table_matches_oracle():
+    import synth
+    np.testing.assert_array_equal(synth.code2_linear(), oracle.code2_linear())
