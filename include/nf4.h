@@ -83,6 +83,16 @@ NF4_API const char* nf4_status_string(nf4_status status);
 NF4_API int nf4_last_cuda_error(void);
 
 /*
+ * nf4_device_error_flags -- read and clear the library's device-side error
+ * flags. Bit 0 is set when a kernel's bounded wait for its own asynchronous
+ * global->shared copies ran out (about one second); that kernel then writes
+ * NaN to the outputs it owns and returns instead of hanging. Synchronises
+ * with the device (cudaMemcpyFromSymbol). `flags` is a host pointer.
+ * Errors: NF4_ERR_NULL, NF4_ERR_CUDA.
+ */
+NF4_API nf4_status nf4_device_error_flags(unsigned int* flags);
+
+/*
  * nf4_dequant -- expand n NF4 elements to bfloat16 or binary16.
  * Defined by "NF4 双重量化反量化 CUDA Kernel 实现报告", section 1.3 (formula)
  * and section 2.2 (nibble order); see the format notes above.

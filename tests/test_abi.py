@@ -29,7 +29,8 @@ def declared_functions():
 def test_exports_every_declared_symbol(lib):
     names = declared_functions()
     assert set(names) == {"nf4_version", "nf4_status_string", "nf4_last_cuda_error", "nf4_dequant",
-                          "nf4_gemv", "nf4_quantize_workspace_size", "nf4_quantize"}
+                          "nf4_gemv", "nf4_quantize_workspace_size", "nf4_quantize",
+                          "nf4_device_error_flags"}
     for n in names:
         assert hasattr(lib, n), n
 
@@ -44,6 +45,7 @@ def test_status_strings_and_version(lib):
     assert lib.nf4_status_string(99).decode().startswith("NF4: unknown")
     assert lib.nf4_version() == 100
     assert lib.nf4_last_cuda_error() == 0
+    assert lib.nf4_device_error_flags(None) == ERR_NULL
 
 
 A = 0x100000  # a fake, well-aligned address: never dereferenced by these calls

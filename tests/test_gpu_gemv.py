@@ -111,3 +111,16 @@ def test_special_inputs():
     y = gpu_gemv(t, N, K, x)
     for b, c in enumerate(cols):
         np.testing.assert_allclose(y[b], W[:, c], rtol=1e-3, atol=1e-6)
+
+
+def test_no_device_error_flags_after_gemv():
+    """No bounded wait of the streaming GEMV ran out during the tests above."""
+    import w4a16_gemv_gb300 as nf4
+    N, K = 4096, 4096
+    w = synth.weights(990, N * K)
+    t = oracle.quantize(w, 64, 256, synth.code2_linear())
+    x = synth.activations(991, 1, K)
+    y = gpu_gemv(t, N, K, x)
+    assert nf4.nf4_device_error_flags() == 0
+    y_ref, s_abs = oracle.gemv(t, N, K, x)
+    assert_gemv_close(y, y_ref, s_abs)

@@ -15,7 +15,8 @@ from dataclasses import dataclass
 import torch
 
 __all__ = ["NF4Error", "NF4Weight", "nf4_dequant", "nf4_gemv", "nf4_quantize",
-           "nf4_quantize_workspace_size", "nf4_version", "nf4_status_string", "LIB_PATH"]
+           "nf4_quantize_workspace_size", "nf4_version", "nf4_status_string",
+           "nf4_device_error_flags", "LIB_PATH"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libnf4.so")
 
@@ -38,6 +39,8 @@ _lib.nf4_quantize_workspace_size.argtypes = [_I64, _I32, _I32]
 _lib.nf4_quantize_workspace_size.restype = ctypes.c_size_t
 _lib.nf4_quantize.argtypes = [_P, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
 _lib.nf4_quantize.restype = ctypes.c_int
+_lib.nf4_device_error_flags.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+_lib.nf4_device_error_flags.restype = ctypes.c_int
 
 NF4_BF16 = 0
 NF4_FP16 = 1
@@ -60,6 +63,13 @@ def nf4_version() -> int:
 
 def nf4_status_string(status: int) -> str:
     return _lib.nf4_status_string(int(status)).decode()
+
+
+def nf4_device_error_flags() -> int:
+    """Read and clear the device-side error flags (bit 0: a bounded wait ran out)."""
+    f = ctypes.c_uint(0)
+    _check(_lib.nf4_device_error_flags(ctypes.byref(f)), "nf4_device_error_flags")
+    return int(f.value)
 
 
 def _check(status: int, where: str) -> None:

@@ -79,6 +79,11 @@ const char* nf4_status_string(nf4_status status) {
 
 int nf4_last_cuda_error(void) { return g_last_cuda_error; }
 
+nf4_status nf4_device_error_flags(unsigned int* flags) {
+  if (!flags) return NF4_ERR_NULL;
+  return cuda_status(nf4::read_and_clear_device_flags(flags));
+}
+
 nf4_status nf4_dequant(const uint8_t* packed, const uint8_t* absmax_q, const uint16_t* absmax2,
                        const uint16_t* code2, float offset, int64_t n, int32_t blocksize,
                        int32_t s2_blocksize, void* out, nf4_dtype out_dtype,

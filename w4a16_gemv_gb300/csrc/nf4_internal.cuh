@@ -7,17 +7,35 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "nf4.h"
 
 namespace nf4 {
 
 // The NF4 code book: the sixteen 8-digit values printed in
-// "NF4反量化算子优化", section "NF4 table", as binary32.
-static __constant__ float kCode[16] = {
-    -1.00000000f, -0.69619280f, -0.52507305f, -0.39491749f,
-    -0.28444138f, -0.18477343f, -0.09105004f, 0.00000000f,
-    0.07958030f,  0.16093020f,  0.24611230f,  0.33791524f,
-    0.44070983f,  0.56261700f,  0.72295684f,  1.00000000f};
+// "NF4反量化算子优化", section "NF4 table", as binary32. Code j (0..15) is
+// selected from immediates, without touching memory (a first access to
+// __constant__ data costs each SM a DRAM round trip).
+__device__ __forceinline__ float nf4_code_select(int j) {
+  float v = -1.00000000f;
+  v = (j == 1) ? -0.69619280f : v;
+  v = (j == 2) ? -0.52507305f : v;
+  v = (j == 3) ? -0.39491749f : v;
+  v = (j == 4) ? -0.28444138f : v;
+  v = (j == 5) ? -0.18477343f : v;
+  v = (j == 6) ? -0.09105004f : v;
+  v = (j == 7) ? 0.00000000f : v;
+  v = (j == 8) ? 0.07958030f : v;
+  v = (j == 9) ? 0.16093020f : v;
+  v = (j == 10) ? 0.24611230f : v;
+  v = (j == 11) ? 0.33791524f : v;
+  v = (j == 12) ? 0.44070983f : v;
+  v = (j == 13) ? 0.56261700f : v;
+  v = (j == 14) ? 0.72295684f : v;
+  v = (j == 15) ? 1.00000000f : v;
+  return v;
+}
 
 // Arguments common to every entry point that reads a quantized tensor.
 struct QuantTensor {
@@ -70,5 +88,136 @@ size_t quantize_workspace_bytes(int64_t n, int lbs, int ls2);
 cudaError_t launch_quantize(const float* w, int64_t n, int lbs, int ls2, const uint16_t* code2,
                             uint8_t* packed, uint8_t* absmax_q, uint16_t* absmax2,
                             float* offset, void* workspace, cudaStream_t stream);
+
+}  // namespace nf4
+
+namespace nf4 {
+
+// ---------------------------------------------------------------------------
+// Bulk asynchronous copies (cp.async.bulk) completing on shared-memory
+// mbarriers, for sm_90+ (used on sm_103a).
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+// Makes mbarrier initialisation visible to the asynchronous proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// Global -> shared bulk copy of `bytes` (multiple of 16, both addresses
+// 16-byte aligned); completion is signalled on `bar` as transaction bytes.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
+                                              uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Bulk prefetch of global memory into L2 (size a multiple of 16, address
+// 16-byte aligned).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for phase `parity` of `bar`, giving up after about `limit_cycles`
+// SM clock cycles. Returns false on timeout (the caller reports it).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  long long limit_cycles) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > limit_cycles) return false;
+  }
+  return true;
+}
+
+// A wait on the library's own asynchronous copies that exceeds this many SM
+// cycles (about one second at 2 GHz) is reported instead of spinning on.
+constexpr long long kWaitLimitCycles = 2000000000ll;
+
+// Device-side error flags (bit 0: a bounded wait timed out). Read and cleared
+// by nf4_device_error_flags().
+cudaError_t read_and_clear_device_flags(unsigned int* flags);
+
+}  // namespace nf4
+
+namespace nf4 {
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch. Kernels of this library are launched with
+// programmatic stream serialisation allowed, so a kernel can be scheduled
+// while the previous kernel in the stream is still finishing. Each kernel
+// therefore (1) signals its own dependents early and (2) waits for the
+// previous grid's completion and memory flush before its first global
+// memory access; work before that point touches only registers, shared
+// memory and the constant bank.
+#ifndef NF4_USE_PDL
+#define NF4_USE_PDL 1
+#endif
+
+__device__ __forceinline__ void pdl_wait_prior_grid() {
+#if NF4_USE_PDL
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+#endif
+}
+
+__device__ __forceinline__ void pdl_allow_dependents() {
+#if NF4_USE_PDL
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#endif
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k_pdl(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                         cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = (NF4_USE_PDL && pdl) ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// Launch with programmatic stream serialisation allowed.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t stream, Args&&... args) {
+  return launch_k_pdl(true, kernel, grid, block, smem, stream, std::forward<Args>(args)...);
+}
 
 }  // namespace nf4

@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(kThreads) absmax_encode_kernel(const float* __
                                                                  uint8_t* __restrict__ packed,
                                                                  float* __restrict__ absmax) {
   __shared__ float sT[16];
-  if (threadIdx.x < 16) sT[threadIdx.x] = kCode[threadIdx.x];
+  if (threadIdx.x < 16) sT[threadIdx.x] = nf4_code_select(int(threadIdx.x));
   __syncthreads();
   const int lane = threadIdx.x & 31;
   const int64_t bs = int64_t(1) << lbs;
