@@ -28,7 +28,8 @@
  * Conventions for every entry point:
  *   - All array arguments are DEVICE pointers owned by the caller; the library
  *     never allocates, frees or keeps them, and keeps no global state beyond
- *     a per-device cache of the SM count.
+ *     a per-device cache of the SM count and the fixed device scratch array of
+ *     nf4_quantize_noalloc.
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *     stream) and the call returns without synchronising.
  *   - Argument checks run on the host before any launch; on failure nothing
@@ -187,6 +188,41 @@ NF4_API nf4_status nf4_quantize(const float* w, int64_t n, int32_t blocksize, in
                         const uint16_t* code2, uint8_t* packed, uint8_t* absmax_q,
                         uint16_t* absmax2, float* offset, void* workspace,
                         size_t workspace_bytes, nf4_stream_t stream);
+
+/* Size in bytes of the fixed device scratch array of nf4_quantize_noalloc:
+ * 16 MiB + 128 KiB, the nf4_quantize workspace of n = 2^28 elements at
+ * blocksize 64, s2_blocksize 256. */
+#define NF4_QUANTIZE_NOALLOC_SCRATCH_BYTES 16908288
+
+/*
+ * nf4_quantize_noalloc -- nf4_quantize with its workspace taken from a fixed
+ * device array inside the library instead of caller memory. The pages have no
+ * counterpart: it is an interface variant for callers that cannot allocate
+ * device memory (hosts with no device allocator of their own, and code that
+ * must not call cudaMalloc/cudaFree because they may synchronise the device).
+ * It allocates and frees nothing. Results are identical to nf4_quantize.
+ *
+ *   Arguments, layout and definition: as for nf4_quantize, without
+ *   `workspace` / `workspace_bytes`.
+ *   Limit: nf4_quantize_workspace_size(n, blocksize, s2_blocksize) must not
+ *     exceed NF4_QUANTIZE_NOALLOC_SCRATCH_BYTES (n <= 2^28 at blocksize 64,
+ *     s2_blocksize 256); larger inputs return NF4_ERR_WORKSPACE before any
+ *     CUDA call.
+ *   Set-up: the first call on each device (with that device current) looks up
+ *     the array's device address with cudaGetSymbolAddress and caches it; make
+ *     that first call before any stream capture.
+ *   Concurrency: the array is shared by all callers on a device, so calls
+ *     whose kernels may overlap in time (different streams, or host threads
+ *     without an ordering between their streams) race on it; the caller
+ *     serialises them. Calls on one stream are ordered and safe.
+ * Errors: NF4_ERR_NULL, NF4_ERR_INVALID_SIZE, NF4_ERR_UNSUPPORTED_BLOCKSIZE,
+ *   NF4_ERR_MISALIGNED, NF4_ERR_WORKSPACE (input too large for the array),
+ *   NF4_ERR_CUDA.
+ */
+NF4_API nf4_status nf4_quantize_noalloc(const float* w, int64_t n, int32_t blocksize,
+                                        int32_t s2_blocksize, const uint16_t* code2,
+                                        uint8_t* packed, uint8_t* absmax_q, uint16_t* absmax2,
+                                        float* offset, nf4_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -30,7 +30,7 @@ def test_exports_every_declared_symbol(lib):
     names = declared_functions()
     assert set(names) == {"nf4_version", "nf4_status_string", "nf4_last_cuda_error", "nf4_dequant",
                           "nf4_gemv", "nf4_quantize_workspace_size", "nf4_quantize",
-                          "nf4_device_error_flags"}
+                          "nf4_device_error_flags", "nf4_quantize_noalloc"}
     for n in names:
         assert hasattr(lib, n), n
 
@@ -117,3 +117,24 @@ def test_quantize_argument_errors_and_workspace_size(lib):
     assert q(ws_ptr=0) == ERR_WS
     assert q(ws_bytes=16) == ERR_WS
     assert q(ws_ptr=A + 4) == ERR_WS
+
+
+def test_quantize_noalloc_argument_errors_and_limit(lib):
+    text = open(HEADER).read()
+    limit = int(re.search(r"#define NF4_QUANTIZE_NOALLOC_SCRATCH_BYTES (\d+)", text).group(1))
+    lib.nf4_quantize_workspace_size.restype = ctypes.c_size_t
+    # the stated limit is exactly the workspace of 2^28 elements at 64/256
+    assert lib.nf4_quantize_workspace_size(1 << 28, 64, 256) == limit
+    assert lib.nf4_quantize_workspace_size((1 << 28) + 1, 64, 256) > limit
+
+    def q(n=1000, w=A, off=A, bs=64, s2=256):
+        return lib.nf4_quantize_noalloc(P(w), n, bs, s2, P(A), P(A), P(A), P(A), P(off), None)
+    assert q(n=-1) == ERR_SIZE
+    assert q(bs=5) == ERR_BS
+    assert q(n=0, w=0) == OK
+    assert q(w=0) == ERR_NULL
+    assert q(off=0) == ERR_NULL
+    assert q(w=A + 2) == ERR_ALIGN
+    # too large for the fixed scratch: rejected on the host before any CUDA call
+    assert q(n=(1 << 28) + 1) == ERR_WS
+    assert q(n=1 << 30, bs=2, s2=1) == ERR_WS

@@ -15,7 +15,7 @@ from dataclasses import dataclass
 import torch
 
 __all__ = ["NF4Error", "NF4Weight", "nf4_dequant", "nf4_gemv", "nf4_quantize",
-           "nf4_quantize_workspace_size", "nf4_version", "nf4_status_string",
+           "nf4_quantize_workspace_size", "nf4_quantize_noalloc", "nf4_version", "nf4_status_string",
            "nf4_device_error_flags", "LIB_PATH"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libnf4.so")
@@ -39,6 +39,8 @@ _lib.nf4_quantize_workspace_size.argtypes = [_I64, _I32, _I32]
 _lib.nf4_quantize_workspace_size.restype = ctypes.c_size_t
 _lib.nf4_quantize.argtypes = [_P, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
 _lib.nf4_quantize.restype = ctypes.c_int
+_lib.nf4_quantize_noalloc.argtypes = [_P, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P]
+_lib.nf4_quantize_noalloc.restype = ctypes.c_int
 _lib.nf4_device_error_flags.argtypes = [ctypes.POINTER(ctypes.c_uint)]
 _lib.nf4_device_error_flags.restype = ctypes.c_int
 
@@ -187,6 +189,28 @@ def nf4_quantize(w: torch.Tensor, code2: torch.Tensor, blocksize: int = 64, s2_b
                            offset.data_ptr(), _ptr(workspace, "workspace", torch.uint8),
                            workspace.numel(), _stream(stream))
     _check(st, "nf4_quantize")
+    return NF4Weight(packed, absmax_q, absmax2, code2, float(offset.item()) if n > 0 else 0.0, n,
+                     tuple(w.shape), blocksize, s2_blocksize)
+
+
+def nf4_quantize_noalloc(w: torch.Tensor, code2: torch.Tensor, blocksize: int = 64,
+                         s2_blocksize: int = 256, stream=None) -> NF4Weight:
+    """nf4_quantize with the library's fixed device scratch (no workspace argument)."""
+    n = w.numel()
+    nbytes, nb, ng = _sizes(n, blocksize, s2_blocksize) if n > 0 else (0, 0, 0)
+    dev = w.device
+    packed = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    absmax_q = torch.empty(nb, dtype=torch.uint8, device=dev)
+    absmax2 = torch.empty(ng, dtype=torch.float16, device=dev)
+    offset = torch.zeros(1, dtype=torch.float32, device=dev)
+    st = _lib.nf4_quantize_noalloc(_ptr(w.reshape(-1), "w", torch.float32, n),
+                                   int(n), int(blocksize), int(s2_blocksize),
+                                   _ptr(code2, "code2", torch.float16, 256),
+                                   _ptr(packed, "packed", torch.uint8),
+                                   _ptr(absmax_q, "absmax_q", torch.uint8),
+                                   _ptr(absmax2, "absmax2", torch.float16),
+                                   offset.data_ptr(), _stream(stream))
+    _check(st, "nf4_quantize_noalloc")
     return NF4Weight(packed, absmax_q, absmax2, code2, float(offset.item()) if n > 0 else 0.0, n,
                      tuple(w.shape), blocksize, s2_blocksize)
 

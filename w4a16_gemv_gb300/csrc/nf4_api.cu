@@ -153,4 +153,25 @@ nf4_status nf4_quantize(const float* w, int64_t n, int32_t blocksize, int32_t s2
                                           workspace, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+nf4_status nf4_quantize_noalloc(const float* w, int64_t n, int32_t blocksize,
+                                int32_t s2_blocksize, const uint16_t* code2, uint8_t* packed,
+                                uint8_t* absmax_q, uint16_t* absmax2, float* offset,
+                                nf4_stream_t stream) {
+  if (n < 0 || n > kMaxElems) return NF4_ERR_INVALID_SIZE;
+  int lbs = 0, ls2 = 0;
+  nf4_status st = check_block_sizes(blocksize, s2_blocksize, &lbs, &ls2);
+  if (st != NF4_OK) return st;
+  if (n == 0) return NF4_OK;
+  if (!w || !code2 || !packed || !absmax_q || !absmax2 || !offset) return NF4_ERR_NULL;
+  if (!aligned(w, 4) || !aligned(code2, 2) || !aligned(absmax2, 2) || !aligned(offset, 4))
+    return NF4_ERR_MISALIGNED;
+  if (nf4::quantize_workspace_bytes(n, lbs, ls2) > size_t(NF4_QUANTIZE_NOALLOC_SCRATCH_BYTES))
+    return NF4_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  const cudaError_t e = nf4::quantize_static_scratch(&scratch);
+  if (e != cudaSuccess) return cuda_status(e);
+  return cuda_status(nf4::launch_quantize(w, n, lbs, ls2, code2, packed, absmax_q, absmax2, offset,
+                                          scratch, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

@@ -88,6 +88,9 @@ size_t quantize_workspace_bytes(int64_t n, int lbs, int ls2);
 cudaError_t launch_quantize(const float* w, int64_t n, int lbs, int ls2, const uint16_t* code2,
                             uint8_t* packed, uint8_t* absmax_q, uint16_t* absmax2,
                             float* offset, void* workspace, cudaStream_t stream);
+// Device address of the fixed nf4_quantize_noalloc scratch on the current
+// device (NF4_QUANTIZE_NOALLOC_SCRATCH_BYTES bytes, 256-byte aligned).
+cudaError_t quantize_static_scratch(void** ptr);
 
 }  // namespace nf4
 

@@ -21,6 +21,8 @@
 //   3. finalize_offset: one thread, binary64 sum of the group sums in order,
 //      divided by the block count, rounded to binary32.
 //   4. second_level: one warp per group -- absmax2 and absmax_q.
+#include <mutex>
+
 #include "nf4_internal.cuh"
 
 namespace nf4 {
@@ -188,6 +190,47 @@ cudaError_t launch_quantize(const float* w, int64_t n, int lbs, int ls2, const u
   second_level_kernel<<<dim3(unsigned(grid_for(ng, kWarps, sms))), kThreads, 0, stream>>>(
       absmax, nb, ls2, code2, offset, absmax2, absmax_q);
   return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Fixed scratch for nf4_quantize_noalloc: the same four kernels, with the
+// block-absmax / group-sum workspace in a file-scope device array instead of
+// caller memory. It serves callers that cannot allocate device memory: hosts
+// with no device allocator of their own (plain C programs without a caching
+// allocator) and code that must not call cudaMalloc/cudaFree, which may
+// synchronise the device and stall work queued on other streams. The array is
+// fully overwritten before it is read (every block absmax and every group sum
+// is written by the first two kernels), so nothing has to be cleared. It is
+// one array per device, shared by every caller: calls that overlap in time
+// (different streams, or different host threads without an ordering between
+// their streams) race on it and must be serialised by the caller.
+namespace {
+
+__device__ __align__(256) unsigned char g_quantize_scratch[NF4_QUANTIZE_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+}  // namespace
+
+// Device address of g_quantize_scratch on the current device. The first call
+// on a device looks it up with cudaGetSymbolAddress (which may load this
+// translation unit's module); later calls read the per-device cache.
+cudaError_t quantize_static_scratch(void** ptr) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_quantize_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_ptr[dev] = p;
+  }
+  *ptr = g_scratch_ptr[dev];
+  return cudaSuccess;
 }
 
 }  // namespace nf4
