@@ -171,6 +171,12 @@ constexpr long long kWaitLimitCycles = 2000000000ll;
 // Device-side error flags (bit 0: a bounded wait timed out). Read and cleared
 // by nf4_device_error_flags().
 cudaError_t read_and_clear_device_flags(unsigned int* flags);
+cudaError_t read_and_clear_b1_flags(unsigned int* flags);
+
+// Batch-1 GEMV (k-stationary, bulk-copy pipelined). Sets *done when it
+// handled the call; otherwise the caller uses the general kernels.
+cudaError_t try_gemv_b1(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x, float* y,
+                        int sms, cudaStream_t stream, bool* done);
 
 }  // namespace nf4
 
