@@ -21,13 +21,12 @@
 //     needed. (On this GPU a 1-D bulk copy costs about one memory latency of
 //     copy-engine time per copy, so copies under ~32 KB cannot stream a CTA's
 //     rows at full bandwidth.)
-//   * Before the grid-dependency wait, one thread asks L2 to prefetch the
-//     CTA's inputs (a hint: L2 is the point of coherence, so data written by
-//     the preceding kernel is still seen by the loads after the wait); after
-//     it, the small loads (x, code2, absmax2, absmax_q) go out together, and
-//     the first weight steps once they have arrived and x is converted (loads
-//     queue per SM, so small loads next to a weight stream would wait behind
-//     it); the block scales of the CTA are decoded once into shared memory.
+//   * After the grid-dependency wait the small loads (x, code2, absmax2, absmax_q) go out together (as
+//     volatile loads, so the compiler keeps them ahead of the weight stream),
+//     and the first weight steps once they have arrived and x is converted
+//     (loads queue per SM, so a small load issued next to a weight stream
+//     would wait behind it); the block scales of the CTA are decoded once
+//     into shared memory.
 //   * Inner loop per packed byte: one byte permute forms the complete shared
 //     address of the byte's entry in a lane-private table of binary16 code
 //     pairs (table at a 64 KB-aligned shared address, 256-byte rows, lane l at
@@ -48,9 +47,6 @@ namespace {
 
 #ifndef NF4_B1_RPG
 #define NF4_B1_RPG 4
-#endif
-#ifndef NF4_B1_PREFETCH
-#define NF4_B1_PREFETCH 0
 #endif
 
 constexpr int kThreads = 512;
@@ -370,26 +366,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_b1_kernel(const B1Args p) {
   const int rg1 = consumer ? group_row0(nrows, p.G, g + 1) : 0;
   const uint8_t* lane_src = slab + int64_t(cc) * CB;
 
-#if NF4_B1_PREFETCH
-  if (tid == 0) {
-    // Warm L2 (hint only; see above): the small inputs first, rounded out to
-    // 16-byte blocks (a 16-byte block never crosses a page, so it is mapped
-    // when one of its bytes is), then the weight slab.
-    auto prefetch_out = [](const void* lo, const void* hi) {
-      const uintptr_t a0 = reinterpret_cast<uintptr_t>(lo) & ~uintptr_t(15);
-      const uintptr_t a1 = (reinterpret_cast<uintptr_t>(hi) + 15u) & ~uintptr_t(15);
-      for (uintptr_t a = a0; a < a1; a += 65536u)
-        bulk_prefetch_l2(reinterpret_cast<const void*>(a), uint32_t(a1 - a < 65536u ? a1 - a : 65536u));
-    };
-    prefetch_out(x, x + K);
-    prefetch_out(t.absmax_q + b0, t.absmax_q + b0 + nq);
-    prefetch_out(t.absmax2 + g0, t.absmax2 + g0 + ng);
-    prefetch_out(t.code2, t.code2 + 256);
-#if NF4_B1_PREFETCH == 1
-    prefetch_out(slab, slab + int64_t(nrows) * row_bytes);
-#endif
-  }
-#endif
   pdl_wait_prior_grid();
 
   // First round of loads, all issued before any is consumed: x pieces (4 per
@@ -503,8 +479,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_b1_kernel(const B1Args p) {
     }
   }
   // The first three weight steps go out once this thread's small loads have
-  // arrived and x is converted: loads queue per SM, so small loads issued
-  // next to a weight stream would wait behind it.
+  // arrived and its x pieces are converted: loads queue per SM, so a small
+  // load issued next to a weight stream would wait behind it.
+  asm volatile("" ::: "memory");  // keep the weight loads after the stores above
   Step<CB, RPG> A, B, C;
   const int n_rows = rg1 - rg0;
   const int n_steps = (n_rows + RPG - 1) / RPG;
