@@ -49,8 +49,6 @@ namespace {
 #define NF4_B1_RPG 4
 #endif
 
-constexpr int kThreads = 512;
-constexpr int kWarps = kThreads / 32;
 constexpr int kMaxGroups = 15;         // named barriers 1..15
 constexpr uint32_t kTabBytes = 65536;  // 256 rows of 256 B
 constexpr int kMaxSmemPerCta = 227 * 1024;
@@ -112,16 +110,18 @@ __device__ __forceinline__ void named_barrier(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-// acc_a += T(low half) * x0, acc_b += T(high half) * x1; binary16 inputs,
-// binary32 accumulation (the products are exact).
-__device__ __forceinline__ void fma2_f16_f32(uint32_t tpair, unsigned short x0, unsigned short x1,
-                                             float& acc_a, float& acc_b) {
-  asm("{\n\t.reg .f16 t0, t1;\n\t"
+// acc_a += T(low half) * x(low half), acc_b += T(high half) * x(high half):
+// binary16 inputs (code pair and x pair, each packed in 32 bits), binary32
+// accumulation (the products are exact).
+__device__ __forceinline__ void fma2_f16_f32(uint32_t tpair, uint32_t xpair, float& acc_a,
+                                             float& acc_b) {
+  asm("{\n\t.reg .f16 t0, t1, x0, x1;\n\t"
       "mov.b32 {t0, t1}, %2;\n\t"
-      "fma.rn.f32.f16 %0, t0, %3, %0;\n\t"
-      "fma.rn.f32.f16 %1, t1, %4, %1;\n\t}"
+      "mov.b32 {x0, x1}, %3;\n\t"
+      "fma.rn.f32.f16 %0, t0, x0, %0;\n\t"
+      "fma.rn.f32.f16 %1, t1, x1, %1;\n\t}"
       : "+f"(acc_a), "+f"(acc_b)
-      : "r"(tpair), "h"(x0), "h"(x1));
+      : "r"(tpair), "r"(xpair));
 }
 
 __device__ __forceinline__ float2 half2_bits_to_float2(uint32_t h) {
@@ -204,8 +204,7 @@ __device__ __forceinline__ void load_step(Step<CB, RPG>& st, const uint8_t* p, u
 // binary16 code pairs; otherwise binary32 x and packed binary32 FMAs.
 template <int CB, bool kFast>
 __device__ __forceinline__ float row_dot(const uint32_t (&w)[CB / 4], uint32_t lanebase,
-                                         uint32_t tab_s, uint32_t lane4,
-                                         const unsigned short (&x16)[2 * CB],
+                                         uint32_t tab_s, uint32_t lane4, const uint32_t (&x16)[CB],
                                          const float2 (&xf)[CB]) {
   if constexpr (kFast) {
     float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
@@ -216,8 +215,8 @@ __device__ __forceinline__ float row_dot(const uint32_t (&w)[CB / 4], uint32_t l
         const uint32_t addr = __byte_perm(w[wi], lanebase, 0x7604u | (uint32_t(i) << 4));
         const uint32_t h = lds_u32(addr);
         const int k = 4 * wi + i;
-        if (i & 1) fma2_f16_f32(h, x16[2 * k], x16[2 * k + 1], a2, a3);
-        else fma2_f16_f32(h, x16[2 * k], x16[2 * k + 1], a0, a1);
+        if (i & 1) fma2_f16_f32(h, x16[k], a2, a3);
+        else fma2_f16_f32(h, x16[k], a0, a1);
       }
     }
     return (a0 + a1) + (a2 + a3);
@@ -241,7 +240,7 @@ __device__ __forceinline__ float row_dot(const uint32_t (&w)[CB / 4], uint32_t l
 template <int CB>
 struct Lane {
   uint32_t lanebase, tab_s, lane4;
-  unsigned short x16[2 * CB];
+  uint32_t x16[CB];  // binary16 x pairs (element 2k in the low half)
   float2 xf[CB];
   float xs;  // power of two undoing the x scaling of this chunk (fast path)
   bool act;  // this lane owns a real chunk
@@ -307,7 +306,7 @@ __device__ __forceinline__ void consume(const B1Args& p, const uint8_t* lane_src
   }
 }
 
-template <int CB, int RPG>
+template <int CB, int RPG, int kThreads>
 __global__ void __launch_bounds__(kThreads, 1) gemv_b1_kernel(const B1Args p) {
   constexpr int CE = 2 * CB;  // elements per column chunk
   extern __shared__ __align__(128) unsigned char smem[];
@@ -323,8 +322,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_b1_kernel(const B1Args p) {
   {
     const uint32_t my_code16 = __half_as_ushort(__float2half_rn(nf4_code_select(lane & 15)));
 #pragma unroll
-    for (int j = 0; j < 256 * 8 / kThreads; ++j) {
+    for (int j = 0; j < (256 * 8 + kThreads - 1) / kThreads; ++j) {
       const int i = tid + j * kThreads;
+      if (i >= 256 * 8) break;  // warp-uniform (all sizes are multiples of 32)
       const int e = i >> 3, q = i & 7;
       const uint32_t hi = __shfl_sync(0xffffffffu, my_code16, e >> 4);
       const uint32_t lo = __shfl_sync(0xffffffffu, my_code16, e & 15);
@@ -518,12 +518,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_b1_kernel(const B1Args p) {
     for (int q = 0; q < CE / 8; ++q) {
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
       if (act) v = lds_u128(L.tab_s + x16_offset<CB>(cc) + uint32_t(q) * 16u);
-      const uint32_t hw[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        L.x16[8 * q + 2 * j] = (unsigned short)(hw[j] & 0xffffu);
-        L.x16[8 * q + 2 * j + 1] = (unsigned short)(hw[j] >> 16);
-      }
+      L.x16[4 * q + 0] = v.x;
+      L.x16[4 * q + 1] = v.y;
+      L.x16[4 * q + 2] = v.z;
+      L.x16[4 * q + 3] = v.w;
     }
     consume<CB, RPG, true>(p, lane_src, uint32_t(row_bytes), A, B, C, L, sPart, wg, lane, rg0, rg1);
   } else {
@@ -568,7 +566,8 @@ int reserved_smem_per_block() {
 // The dynamic window starts after the per-block reserved shared memory (the
 // kernel has no static shared variables).
 bool plan_b1(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x, float* y, int cb,
-             int sms, B1Plan* plan) {
+             int threads, int sms, B1Plan* plan) {
+  const int kWarps = threads / 32;
   B1Args* p = &plan->a;
   const int64_t bs = int64_t(1) << t.lbs;
   const int ce = 2 * cb;
@@ -602,7 +601,7 @@ bool plan_b1(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x, floa
   p->off_xs = off;
   off += align_up_u32(uint32_t(cpr * 4), 128);
   p->off_q = off;
-  if (max_nq > int64_t(4) * kThreads * 16) return false;  // one batch of 16-byte loads
+  if (max_nq > int64_t(4) * threads * 16) return false;  // one batch of 16-byte loads
   off += align_up_u32(uint32_t(max_nq + 16), 128);
   p->off_scale = off;
   off += align_up_u32(uint32_t(max_nq * 4), 128);
@@ -615,9 +614,9 @@ bool plan_b1(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x, floa
   return plan->smem_bytes <= uint32_t(kMaxSmemPerCta);
 }
 
-template <int CB>
+template <int CB, int NT>
 cudaError_t launch_b1(const B1Plan& plan, cudaStream_t stream) {
-  auto kern = gemv_b1_kernel<CB, NF4_B1_RPG>;
+  auto kern = gemv_b1_kernel<CB, NF4_B1_RPG, NT>;
   static int attr_set[64] = {0};
   int dev = 0;
   const cudaError_t ed = cudaGetDevice(&dev);
@@ -628,8 +627,8 @@ cudaError_t launch_b1(const B1Plan& plan, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = 1;
   }
-  return launch_k(kern, dim3(unsigned(plan.a.grid)), dim3(unsigned(kThreads)), plan.smem_bytes,
-                  stream, plan.a);
+  return launch_k(kern, dim3(unsigned(plan.a.grid)), dim3(unsigned(NT)), plan.smem_bytes, stream,
+                  plan.a);
 }
 
 }  // namespace
@@ -641,16 +640,17 @@ cudaError_t try_gemv_b1(const QuantTensor& t, int64_t N, int64_t K, const uint16
     return cudaSuccess;
   if (K % 32 != 0) return cudaSuccess;
   // chunk width: 16 bytes unless that leaves more than 10% of the lanes idle
+  // (measured: more, narrower lanes only add per-row overhead)
   const int64_t cpr16 = K / 32;
   const int cb = (double(cpr16) / double((cpr16 + 31) / 32 * 32) >= 0.9) ? 16 : 8;
   B1Plan p;
-  if (cb == 16 && plan_b1(t, N, K, x, y, 16, sms, &p)) {
+  if (cb == 16 && plan_b1(t, N, K, x, y, 16, 512, sms, &p)) {
     *done = true;
-    return launch_b1<16>(p, stream);
+    return launch_b1<16, 512>(p, stream);
   }
-  if (plan_b1(t, N, K, x, y, 8, sms, &p)) {
+  if (plan_b1(t, N, K, x, y, 8, 512, sms, &p)) {
     *done = true;
-    return launch_b1<8>(p, stream);
+    return launch_b1<8, 512>(p, stream);
   }
   return cudaSuccess;
 }
