@@ -354,9 +354,10 @@ cudaError_t dispatch_batch(const QuantTensor& t, int64_t N, int64_t K, const uin
     if (blocks > int64_t(sms) * 8) blocks = int64_t(sms) * 8;
     return launch_k(zero_fill_kernel, dim3(unsigned(blocks)), dim3(kThreads), 0, stream, y, count);
   }
-  if constexpr (B == 1) {
+  {
     bool done = false;
-    const cudaError_t ek = try_gemv_b1(t, N, K, x, y, sms, stream, &done);
+    const cudaError_t ek = (B == 1) ? try_gemv_b1(t, N, K, x, y, sms, stream, &done)
+                                    : try_gemv_bn(t, N, K, x, B, y, sms, stream, &done);
     if (done || ek != cudaSuccess) return ek;
   }
   const FastConfig f = choose_config(t, N, K, B, x, sms);

@@ -1,4 +1,4 @@
-// nf4_gemv_b1.cu -- batch-1 decode GEMV y = W_hat x with the NF4 double-quant
+// nf4_gemv_stream.cu -- batch-1 decode GEMV y = W_hat x with the NF4 double-quant
 // dequantization fused, for sm_103a.
 //
 // What is computed follows "RTX 4060 上的 LLM 量化实测：4-bit decode 比 FP16 慢在
@@ -188,6 +188,8 @@ __device__ __forceinline__ void load_step(Step<CB, RPG>& st, const uint8_t* p, u
       if constexpr (CB == 16) {
         const uint4 v = ldg_stream_u128(p + r * row_bytes);
         st.w[r][0] = v.x; st.w[r][1] = v.y; st.w[r][2] = v.z; st.w[r][3] = v.w;
+      } else if constexpr (CB == 4) {
+        st.w[r][0] = ldg_stream_u32(p + r * row_bytes);
       } else {
         uint2 v;
         asm volatile("ld.global.nc.L1::no_allocate.v2.b32 {%0,%1}, [%2];"
@@ -631,6 +633,342 @@ cudaError_t launch_b1(const B1Plan& plan, cudaStream_t stream) {
                   plan.a);
 }
 
+
+// ---------------------------------------------------------------------------
+// Batch 2..8. Same layout as batch 1 (k-stationary, direct weight loads, RPG
+// rows per step, three steps in flight), with x kept in binary32 (bfloat16
+// widens exactly, so there is no conversion to check): the lane's x chunk of
+// every vector stays in registers. The code-pair table holds binary32 pairs
+// (lane-private, 256-byte rows, lane l at byte 8l), so one byte permute, one
+// 64-bit shared load and one packed fma.rn.f32x2 per vector handle a packed
+// byte. The kernel runs BP = 2, 4 or 8 vectors (3 runs as 4, 5..7 as 8 with
+// zero vectors that are not written). Rows longer than the CTA's lanes are
+// walked in column slices; a warp adds its reduced partial of every slice to
+// its own (row, vector) slot, so the sums keep a fixed order.
+
+template <int BP, int CB>
+struct LaneN {
+  uint32_t lanebase8;  // (table address & 0xffff0000) | 8 * lane
+  float2 xf[BP][CB];   // x pairs of this lane's chunk, per vector
+  bool act;            // this lane owns a real chunk in the current slice
+  int scol;            // quantization block of the chunk within a row
+};
+
+__device__ __forceinline__ float2 lds_f2(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
+  return v;
+}
+
+// One step (rows r0 .. r0 + rows - 1 of the CTA): per row and vector, the
+// lane's dot product times the block scale; transposed warp reduction over
+// the RPG * BP values; partial added to (or stored in, for the first slice)
+// sPart[(row * BP + vector) * W + warp].
+template <int BP, int CB, int RPG>
+__device__ __forceinline__ void compute_step_n(const Step<CB, RPG>& st, const LaneN<BP, CB>& L,
+                                               const float* sScale, float* sPart, int spr, int W,
+                                               int wg, int lane, int r0, int rows, bool first) {
+  float part[RPG * BP];
+#pragma unroll
+  for (int r = 0; r < RPG; ++r) {
+    float2 acc[BP];
+#pragma unroll
+    for (int b = 0; b < BP; ++b) acc[b] = make_float2(0.f, 0.f);
+    if (rows == RPG || r < rows) {  // warp-uniform
+#pragma unroll
+      for (int wi = 0; wi < CB / 4; ++wi) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t addr = __byte_perm(st.w[r][wi], L.lanebase8, 0x7604u | (uint32_t(i) << 4));
+          const float2 tw = lds_f2(addr);
+          const int k = 4 * wi + i;
+#pragma unroll
+          for (int b = 0; b < BP; ++b) acc[b] = __ffma2_rn(tw, L.xf[b][k], acc[b]);
+        }
+      }
+    }
+    const float sc = (L.act && r < rows) ? sScale[(r0 + r) * spr + L.scol] : 0.0f;
+#pragma unroll
+    for (int b = 0; b < BP; ++b) part[r * BP + b] = sc * (acc[b].x + acc[b].y);
+  }
+  const float red = transposed_warp_reduce<RPG * BP>(part, lane);
+  if (lane < RPG * BP) {
+    const int idx = transposed_index<RPG * BP>(lane);
+    const int r = idx / BP, b = idx - (idx / BP) * BP;
+    if (r < rows) {
+      float* d = sPart + ((r0 + r) * BP + b) * W + wg;
+      *d = first ? red : *d + red;
+    }
+  }
+}
+
+template <int BP, int CB, int RPG>
+__device__ __forceinline__ void consume_n(const uint8_t* lane_src, uint32_t row_bytes,
+                                          Step<CB, RPG>& A, Step<CB, RPG>& B, Step<CB, RPG>& C,
+                                          const LaneN<BP, CB>& L, const float* sScale, float* sPart,
+                                          int spr, int W, int wg, int lane, int rg0, int rg1,
+                                          bool first) {
+  const int n = rg1 - rg0;
+  const int ns = (n + RPG - 1) / RPG;
+  auto rows_of = [&](int s) { return (n - s * RPG < RPG) ? n - s * RPG : RPG; };
+  auto src_of = [&](int s) { return lane_src + uint32_t(rg0 + s * RPG) * row_bytes; };
+  for (int s = 0; s < ns; s += 3) {
+    compute_step_n<BP, CB, RPG>(A, L, sScale, sPart, spr, W, wg, lane, rg0 + s * RPG, rows_of(s), first);
+    if (s + 3 < ns) load_step<CB, RPG>(A, src_of(s + 3), row_bytes, rows_of(s + 3));
+    if (s + 1 < ns) {
+      compute_step_n<BP, CB, RPG>(B, L, sScale, sPart, spr, W, wg, lane, rg0 + (s + 1) * RPG,
+                                  rows_of(s + 1), first);
+      if (s + 4 < ns) load_step<CB, RPG>(B, src_of(s + 4), row_bytes, rows_of(s + 4));
+    }
+    if (s + 2 < ns) {
+      compute_step_n<BP, CB, RPG>(C, L, sScale, sPart, spr, W, wg, lane, rg0 + (s + 2) * RPG,
+                                  rows_of(s + 2), first);
+      if (s + 5 < ns) load_step<CB, RPG>(C, src_of(s + 5), row_bytes, rows_of(s + 5));
+    }
+  }
+}
+
+// Arguments of the batched kernel.
+struct BNArgs {
+  QuantTensor t;
+  const uint16_t* x;
+  float* y;
+  int64_t N;
+  int32_t K;
+  int batch;   // real vectors (<= BP)
+  int grid;    // CTAs; CTA b owns rows [b*N/grid, (b+1)*N/grid)
+  int W;       // warps per row group (per slice)
+  int G;       // row groups
+  int spr;     // quantization blocks per row
+  int cpr;     // column chunks per row
+  int slices;  // column slices of W * 32 chunks
+  uint32_t off_c2, off_a2, off_q, off_scale, off_part, off_tab;
+};
+
+template <int BP, int CB, int RPG>
+__global__ void __launch_bounds__(512, 1) gemv_bn_kernel(const BNArgs p) {
+  constexpr int kThreads = 512;
+  constexpr int CE = 2 * CB;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+
+  // binary32 pair table at shared window address 64 KB: row e holds
+  // (NF4[e >> 4], NF4[e & 15]) at bytes 8l..8l+7 for every lane l.
+  unsigned char* const tab = smem + (65536u - smem_u32(smem));
+  {
+    const float my_code = nf4_code_select(lane & 15);
+#pragma unroll
+    for (int j = 0; j < 256 * 16 / kThreads; ++j) {
+      const int i = tid + j * kThreads;
+      const int e = i >> 4, q = i & 15;
+      const float hi = __shfl_sync(0xffffffffu, my_code, e >> 4);
+      const float lo = __shfl_sync(0xffffffffu, my_code, e & 15);
+      *reinterpret_cast<float4*>(tab + e * 256 + q * 16) = make_float4(hi, lo, hi, lo);
+    }
+  }
+  pdl_allow_dependents();
+
+  const QuantTensor& t = p.t;
+  const int64_t N = p.N;
+  const int64_t K = p.K;
+  float* sC2 = reinterpret_cast<float*>(smem + p.off_c2);
+  float* sA2 = reinterpret_cast<float*>(smem + p.off_a2);
+  unsigned char* sQ = smem + p.off_q;
+  float* sScale = reinterpret_cast<float*>(smem + p.off_scale);
+  float* sPart = reinterpret_cast<float*>(smem + p.off_part);
+
+  const int64_t row_bytes = K >> 1;
+  const int64_t row_begin = (int64_t(blockIdx.x) * N) / p.grid;
+  const int64_t row_end = (int64_t(blockIdx.x + 1) * N) / p.grid;
+  const int nrows = int(row_end - row_begin);
+  const int64_t b0 = (row_begin * K) >> t.lbs;
+  const int nq = nrows * p.spr;
+  const int64_t g0 = b0 >> t.ls2;
+  const int ng = nq > 0 ? int(((b0 + nq - 1) >> t.ls2) - g0 + 1) : 0;
+  const uint8_t* slab = t.packed + row_begin * row_bytes;
+
+  const int g = warp / p.W;
+  const int wg = warp - g * p.W;
+  const bool consumer = g < p.G;
+  const int rg0 = consumer ? group_row0(nrows, p.G, g) : 0;
+  const int rg1 = consumer ? group_row0(nrows, p.G, g + 1) : 0;
+  pdl_wait_prior_grid();
+
+  // Small loads first (ordered), then the stores that consume them.
+  const uint16_t c2v = tid < 256 ? ldg_u16_ordered(t.code2 + tid) : uint16_t(0);
+  uint16_t av[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int i = tid + j * kThreads;
+    av[j] = i < ng ? ldg_u16_ordered(t.absmax2 + g0 + i) : uint16_t(0);
+  }
+  const uintptr_t qa = reinterpret_cast<uintptr_t>(t.absmax_q + b0);
+  const int q_lead = int(qa & 15u);
+  int q_head = int((16u - (qa & 15u)) & 15u);
+  int q_mid_end = int(((qa + uintptr_t(nq)) & ~uintptr_t(15)) - qa);
+  if (q_mid_end <= q_head) {
+    q_head = nq;
+    q_mid_end = nq;
+  }
+  const int q_vecs = (q_mid_end - q_head) / 16;
+  uint4 qm[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int i = tid + j * kThreads;
+    qm[j] = i < q_vecs ? ldg_v4_ordered(reinterpret_cast<const uint4*>(t.absmax_q + b0 + q_head) + i)
+                       : make_uint4(0u, 0u, 0u, 0u);
+  }
+  int qi = -1;
+  if (tid < q_head) qi = tid;
+  else if (tid >= 32 && tid - 32 < nq - q_mid_end) qi = q_mid_end + (tid - 32);
+  const uint8_t qb = qi >= 0 ? ldg_u8_ordered(t.absmax_q + b0 + qi) : uint8_t(0);
+  if (tid < 256) sC2[tid] = half_bits_to_float(c2v);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int i = tid + j * kThreads;
+    if (i < ng) sA2[i] = half_bits_to_float(av[j]);
+    if (i < q_vecs) *reinterpret_cast<uint4*>(sQ + q_lead + q_head + 16 * i) = qm[j];
+  }
+  if (qi >= 0) sQ[q_lead + qi] = qb;
+  for (int base = 4 * kThreads; base < ng; base += 4 * kThreads) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = base + tid + j * kThreads;
+      av[j] = i < ng ? ldg_u16_ordered(t.absmax2 + g0 + i) : uint16_t(0);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = base + tid + j * kThreads;
+      if (i < ng) sA2[i] = half_bits_to_float(av[j]);
+    }
+  }
+  __syncthreads();
+  {
+    const uint32_t b0g = uint32_t(b0 & ((int64_t(1) << t.ls2) - 1));
+    for (int i = tid; i < nq; i += kThreads)
+      sScale[i] = __fadd_rn(__fmul_rn(sC2[sQ[q_lead + i]], sA2[(b0g + uint32_t(i)) >> t.ls2]), t.offset);
+  }
+  __syncthreads();
+  if (!consumer) return;
+
+  LaneN<BP, CB> L;
+  L.lanebase8 = (smem_u32(tab) & 0xffff0000u) | (uint32_t(lane) << 3);
+  const uint32_t rb = uint32_t(row_bytes);
+  const int n_rows = rg1 - rg0;
+  const int n_steps = (n_rows + RPG - 1) / RPG;
+  auto rows_of = [&](int s) { return (n_rows - s * RPG < RPG) ? n_rows - s * RPG : RPG; };
+  for (int sl = 0; sl < p.slices; ++sl) {
+    const int c = sl * p.W * 32 + wg * 32 + lane;
+    L.act = c < p.cpr;
+    const int cc = L.act ? c : p.cpr - 1;
+    L.scol = int((int64_t(cc) * CE) >> t.lbs);
+    const uint8_t* lane_src = slab + uint32_t(cc) * CB;
+    Step<CB, RPG> A, B, C;
+    if (n_steps > 0) load_step<CB, RPG>(A, lane_src + uint32_t(rg0) * rb, rb, rows_of(0));
+    if (n_steps > 1) load_step<CB, RPG>(B, lane_src + uint32_t(rg0 + RPG) * rb, rb, rows_of(1));
+    if (n_steps > 2) load_step<CB, RPG>(C, lane_src + uint32_t(rg0 + 2 * RPG) * rb, rb, rows_of(2));
+    // x chunk of every vector (bfloat16 -> binary32 exactly); missing
+    // vectors and lanes past the row are zero
+#pragma unroll
+    for (int b = 0; b < BP; ++b) {
+#pragma unroll
+      for (int q = 0; q < CE / 8; ++q) {
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (L.act && b < p.batch)
+          v = __ldg(reinterpret_cast<const uint4*>(p.x + int64_t(b) * K + int64_t(cc) * CE) + q);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          L.xf[b][4 * q + j] = make_float2(__uint_as_float(w[j] << 16), __uint_as_float(w[j] & 0xffff0000u));
+      }
+    }
+    consume_n<BP, CB, RPG>(lane_src, rb, A, B, C, L, sScale, sPart, p.spr, p.W, wg, lane, rg0, rg1,
+                           sl == 0);
+  }
+
+  // End of the group: one sum per (row, vector) over the group's warps.
+  named_barrier(1 + g, p.W * 32);
+  const int gt = tid - g * p.W * 32;
+  for (int idx = gt; idx < n_rows * BP; idx += p.W * 32) {
+    const int r = rg0 + idx / BP, b = idx - (idx / BP) * BP;
+    if (b >= p.batch) continue;
+    float v = 0.0f;
+    for (int w = 0; w < p.W; ++w) v += sPart[(r * BP + b) * p.W + w];
+    p.y[int64_t(b) * N + row_begin + r] = v;
+  }
+}
+
+// Plan for BP vectors and CB-byte chunks (512 threads, one CTA per SM).
+bool plan_bn(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x, int batch, float* y,
+             int bp, int cb, int sms, BNArgs* p, uint32_t* smem_bytes) {
+  const int64_t bs = int64_t(1) << t.lbs;
+  const int ce = 2 * cb;
+  if (N <= 0 || K % 32 != 0 || K % bs != 0 || bs < ce) return false;
+  const int64_t cpr = K / ce;
+  int W = int((cpr + 31) / 32);
+  int slices = 1;
+  if (W > 16) {
+    slices = int((W + 15) / 16);
+    W = int((cpr + 32 * slices - 1) / (32 * slices));
+  }
+  int G = 16 / W;
+  if (G > kMaxGroups) G = kMaxGroups;
+  p->t = t;
+  p->x = x;
+  p->y = y;
+  p->N = N;
+  p->K = int32_t(K);
+  p->batch = batch;
+  p->W = W;
+  p->cpr = int(cpr);
+  p->slices = slices;
+  p->spr = int(K / bs);
+  p->grid = int(N < sms ? N : sms);
+  const int max_rows = int((N + p->grid - 1) / p->grid);
+  if (G > max_rows) G = max_rows;
+  if (slices > 1) G = 1;
+  p->G = G;
+  const int64_t max_nq = int64_t(max_rows) * p->spr;
+  if (max_nq > int64_t(4) * 512 * 16) return false;
+  const int ng_cap = int((max_nq >> t.ls2) + 2);
+  const int res = reserved_smem_per_block();
+  if (res <= 0 || res >= 65536 || res % 256 != 0) return false;
+  uint32_t off = 0;
+  p->off_c2 = off;
+  off += 1024;
+  p->off_a2 = off;
+  off += align_up_u32(uint32_t(ng_cap * 4), 128);
+  p->off_q = off;
+  off += align_up_u32(uint32_t(max_nq + 16), 128);
+  p->off_scale = off;
+  off += align_up_u32(uint32_t(max_nq * 4), 128);
+  p->off_part = off;
+  off += align_up_u32(uint32_t(max_rows * bp * W * 4), 128);
+  const uint32_t tab = 65536u - uint32_t(res);
+  if (off > tab) return false;
+  p->off_tab = tab;
+  *smem_bytes = tab + kTabBytes;
+  return *smem_bytes <= uint32_t(kMaxSmemPerCta);
+}
+
+template <int BP, int CB>
+cudaError_t launch_bn(const BNArgs& a, uint32_t smem_bytes, cudaStream_t stream) {
+  auto kern = gemv_bn_kernel<BP, CB, 2>;
+  static int attr_set[64] = {0};
+  int dev = 0;
+  const cudaError_t ed = cudaGetDevice(&dev);
+  if (ed != cudaSuccess) return ed;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmemPerCta);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = 1;
+  }
+  return launch_k(kern, dim3(unsigned(a.grid)), dim3(512u), smem_bytes, stream, a);
+}
+
 }  // namespace
 
 cudaError_t try_gemv_b1(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x, float* y,
@@ -653,6 +991,30 @@ cudaError_t try_gemv_b1(const QuantTensor& t, int64_t N, int64_t K, const uint16
     return launch_b1<8, 512>(p, stream);
   }
   return cudaSuccess;
+}
+
+cudaError_t try_gemv_bn(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x, int batch,
+                        float* y, int sms, cudaStream_t stream, bool* done) {
+  *done = false;
+  if (batch < 2 || batch > 8) return cudaSuccess;
+  if ((reinterpret_cast<uintptr_t>(t.packed) & 15u) != 0 || (reinterpret_cast<uintptr_t>(x) & 15u) != 0)
+    return cudaSuccess;
+  // x chunk of all BP vectors in registers: BP * 2 CB binary32 values = 64
+  BNArgs a;
+  uint32_t smem = 0;
+  if (batch == 2) {
+    if (!plan_bn(t, N, K, x, batch, y, 2, 16, sms, &a, &smem)) return cudaSuccess;
+    *done = true;
+    return launch_bn<2, 16>(a, smem, stream);
+  }
+  if (batch <= 4) {
+    if (!plan_bn(t, N, K, x, batch, y, 4, 8, sms, &a, &smem)) return cudaSuccess;
+    *done = true;
+    return launch_bn<4, 8>(a, smem, stream);
+  }
+  if (!plan_bn(t, N, K, x, batch, y, 8, 4, sms, &a, &smem)) return cudaSuccess;
+  *done = true;
+  return launch_bn<8, 4>(a, smem, stream);
 }
 
 cudaError_t read_and_clear_b1_flags(unsigned int* flags) {

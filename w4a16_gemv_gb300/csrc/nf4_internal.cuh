@@ -177,6 +177,9 @@ cudaError_t read_and_clear_b1_flags(unsigned int* flags);
 // handled the call; otherwise the caller uses the general kernels.
 cudaError_t try_gemv_b1(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x, float* y,
                         int sms, cudaStream_t stream, bool* done);
+// Batch 2..8 GEMV (k-stationary, binary32 x in registers, column slices).
+cudaError_t try_gemv_bn(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x, int batch,
+                        float* y, int sms, cudaStream_t stream, bool* done);
 
 }  // namespace nf4
 
