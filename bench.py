@@ -305,17 +305,18 @@ def run_native(args, rank, world, local_rank):
 
 def read_traffic(kernel_name):
     """DRAM bytes per launch from the committed ncu summary, if it still
-    matches the current kernel source; else None."""
+    matches the current source of that kernel; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             t = json.load(f)
         import hashlib
-        src = os.path.join(ROOT, "w4a16_gemv_gb300", "csrc", t["source"])
+        k = t["kernels"][kernel_name]
+        src = os.path.join(ROOT, "w4a16_gemv_gb300", "csrc", k["source"])
         h = hashlib.sha256(open(src, "rb").read()).hexdigest()
-        if h != t["source_sha256"]:
+        if h != k["source_sha256"]:
             return None
-        return t["kernels"][kernel_name]["dram_bytes_per_launch"]
+        return k["dram_bytes_per_launch"]
     except Exception:
         return None
 
