@@ -257,23 +257,15 @@ template <int CB, int RPG, bool kFast>
 __device__ __forceinline__ void compute_step(const Step<CB, RPG>& st, const Lane<CB>& L,
                                              float* sPart, int spr, int W, int wg, int lane,
                                              int r0, int rows) {
+  // One code path for full and partial steps (a second path for the last
+  // step made the loop body too large for the instruction cache): rows past
+  // the end are computed from stale registers and dropped.
   float part[RPG];
-  if (rows == RPG) {
-    // full step: no per-row branches, so the rows' table loads interleave
 #pragma unroll
-    for (int r = 0; r < RPG; ++r) {
-      const float sum = row_dot<CB, kFast>(st.w[r], L.lanebase, L.tab_s, L.lane4, L.x16, L.xf);
-      part[r] = L.act ? __fmul_rn(L.scale((r0 + r) * spr + L.scol), L.xs) * sum : 0.0f;
-    }
-  } else {
-#pragma unroll
-    for (int r = 0; r < RPG; ++r) {
-      part[r] = 0.0f;
-      if (r < rows) {  // warp-uniform
-        const float sum = row_dot<CB, kFast>(st.w[r], L.lanebase, L.tab_s, L.lane4, L.x16, L.xf);
-        part[r] = L.act ? __fmul_rn(L.scale((r0 + r) * spr + L.scol), L.xs) * sum : 0.0f;
-      }
-    }
+  for (int r = 0; r < RPG; ++r) {
+    const float sum = row_dot<CB, kFast>(st.w[r], L.lanebase, L.tab_s, L.lane4, L.x16, L.xf);
+    part[r] = (L.act && r < rows) ? __fmul_rn(L.scale((r0 + (r < rows ? r : 0)) * spr + L.scol), L.xs) * sum
+                                  : 0.0f;
   }
   const float red = transposed_warp_reduce<RPG>(part, lane);
   if (lane < RPG) {
@@ -674,7 +666,7 @@ __device__ __forceinline__ void compute_step_n(const Step<CB, RPG>& st, const La
     float2 acc[BP];
 #pragma unroll
     for (int b = 0; b < BP; ++b) acc[b] = make_float2(0.f, 0.f);
-    if (rows == RPG || r < rows) {  // warp-uniform
+    {  // rows past the end are computed from stale registers and dropped
 #pragma unroll
       for (int wi = 0; wi < CB / 4; ++wi) {
 #pragma unroll
@@ -687,9 +679,10 @@ __device__ __forceinline__ void compute_step_n(const Step<CB, RPG>& st, const La
         }
       }
     }
-    const float sc = (L.act && r < rows) ? sScale[(r0 + r) * spr + L.scol] : 0.0f;
+    const bool keep = L.act && r < rows;
+    const float sc = sScale[(r0 + (r < rows ? r : 0)) * spr + L.scol];
 #pragma unroll
-    for (int b = 0; b < BP; ++b) part[r * BP + b] = sc * (acc[b].x + acc[b].y);
+    for (int b = 0; b < BP; ++b) part[r * BP + b] = keep ? sc * (acc[b].x + acc[b].y) : 0.0f;
   }
   const float red = transposed_warp_reduce<RPG * BP>(part, lane);
   if (lane < RPG * BP) {
