@@ -456,6 +456,149 @@ def run_reference(args):
             "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+
+# ---------------------------------------------------------------------------
+# --sweep: every configuration of the workload list timed on its own
+
+def _sweep_time(launch, nsets, reps=5):
+    """us per launch: a CUDA graph of back-to-back launches rotating over the
+    input sets (events only at the graph's ends), best of `reps` replays."""
+    import torch
+    m = max(4 * nsets, 16)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for i in range(nsets):
+            launch(i, s.cuda_stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    e0 = torch.cuda.Event(enable_timing=True, external=True)
+    e1 = torch.cuda.Event(enable_timing=True, external=True)
+    with torch.cuda.stream(s):
+        g.capture_begin()
+        e0.record(s)
+        for i in range(m):
+            launch(i % nsets, s.cuda_stream)
+        e1.record(s)
+        g.capture_end()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    best = None
+    for _ in range(reps):
+        g.replay()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / m
+        best = us if best is None else min(best, us)
+    return best
+
+
+def run_sweep(args):
+    """Times nf4_dequant on configs 0, 1, 2 (standalone dequant of each Qwen
+    layer) and 4, and nf4_gemv on configs 2 and 3 at batch 1/4/8. Inputs are
+    synthetic random codes and scales (timing does not depend on the values);
+    each case rotates over enough input sets to exceed 4x the L2."""
+    import ctypes
+    import numpy as np
+    import torch
+
+    import w4a16_gemv_gb300 as nf4
+    lib = nf4._lib
+    dev = torch.device("cuda:0")
+    peak, peak_kind = load_peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    code2 = torch.from_numpy((((np.arange(256) - 127.5) / 127.5).astype(np.float16))).to(dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(12345)
+    out = []
+
+    def quant_set(n):
+        nb = (n + BS - 1) // BS
+        ng = (nb + S2 - 1) // S2
+        return dict(packed=torch.randint(0, 256, ((n + 1) // 2,), dtype=torch.uint8, device=dev, generator=gen),
+                    absmax_q=torch.randint(0, 256, (nb,), dtype=torch.uint8, device=dev, generator=gen),
+                    absmax2=(torch.rand(ng, device=dev, generator=gen) * 0.04 + 0.01).half())
+
+    def nsets_for(bytes_each, cap=8 << 30):
+        return max(1, min(int(math.ceil(4 * l2 / bytes_each)), max(1, cap // bytes_each)))
+
+    dq_cases = [("cfg0 1024x1024", 1024 * 1024, 0), ("cfg1 4096x4096", 4096 * 4096, 0),
+                ("cfg1 4096x4096", 4096 * 4096, 1)]
+    dq_cases += [(f"cfg2 dequant {nm}", n * k, 0) for nm, n, k in
+                 (("q/o 1536x1536", 1536, 1536), ("k/v 256x1536", 256, 1536),
+                  ("gate/up 8960x1536", 8960, 1536), ("down 1536x8960", 1536, 8960))]
+    dq_cases += [("cfg4 28672x8192", 28672 * 8192, 0)]
+    dq_cases += [(f"cfg4 flat 2^{e}", 1 << e, 0) for e in (20, 22, 24, 26, 28, 30)]
+    dq_cases += [("cfg4 ragged 64*256*1000+64*37", 64 * 256 * 1000 + 64 * 37, 0)]
+    for name, n, dtype in dq_cases:
+        nb = (n + BS - 1) // BS
+        ng = (nb + S2 - 1) // S2
+        bytes_ = (n + 1) // 2 + nb + 2 * ng + 512 + 2 * n
+        r = nsets_for(bytes_)
+        sets = []
+        for _ in range(r):
+            st = quant_set(n)
+            st["out"] = torch.empty(n, dtype=torch.bfloat16 if dtype == 0 else torch.float16, device=dev)
+            sets.append(st)
+
+        def launch(i, sp, n=n, dtype=dtype, sets=sets):
+            st = sets[i]
+            rc = lib.nf4_dequant(st["packed"].data_ptr(), st["absmax_q"].data_ptr(), st["absmax2"].data_ptr(),
+                                 code2.data_ptr(), 0.01, n, BS, S2, st["out"].data_ptr(), dtype, sp)
+            if rc != 0:
+                raise RuntimeError(f"nf4_dequant: {nf4.nf4_status_string(rc)}")
+        us = _sweep_time(launch, r)
+        gbs = bytes_ / us / 1e3
+        out.append({"kind": "dequant", "case": name, "out": "bf16" if dtype == 0 else "fp16", "n": n,
+                    "bytes": bytes_, "us": round(us, 3), "gbs": round(gbs, 1),
+                    "frac_of_measured_hbm": round(gbs / peak, 4), "frac_of_8000": round(gbs / 8000.0, 4),
+                    "sets": r})
+        del sets
+        torch.cuda.empty_cache()
+
+    gv_cases = [("cfg2 q/o", 1536, 1536), ("cfg2 k/v", 256, 1536), ("cfg2 gate/up", 8960, 1536),
+                ("cfg2 down", 1536, 8960), ("cfg3 attn", 4096, 4096), ("cfg3 gate/up", 11008, 4096),
+                ("cfg3 down", 4096, 11008)]
+    for name, N, K in gv_cases:
+        for batch in ((1,) if name.startswith("cfg2") else (1, 4, 8)):
+            n = N * K
+            nb = (n + BS - 1) // BS
+            ng = (nb + S2 - 1) // S2
+            bytes_ = n // 2 + nb + 2 * ng + 512 + 2 * batch * K + 4 * batch * N
+            r = max(2, nsets_for(bytes_))
+            sets = []
+            for _ in range(r):
+                st = quant_set(n)
+                st["x"] = torch.randn(batch, K, device=dev, generator=gen).to(torch.bfloat16)
+                st["y"] = torch.empty(batch, N, device=dev)
+                sets.append(st)
+
+            def launch(i, sp, N=N, K=K, batch=batch, sets=sets):
+                st = sets[i]
+                rc = lib.nf4_gemv(st["packed"].data_ptr(), st["absmax_q"].data_ptr(), st["absmax2"].data_ptr(),
+                                  code2.data_ptr(), 0.01, N, K, BS, S2, st["x"].data_ptr(), batch,
+                                  st["y"].data_ptr(), sp)
+                if rc != 0:
+                    raise RuntimeError(f"nf4_gemv: {nf4.nf4_status_string(rc)}")
+            us = _sweep_time(launch, r)
+            gbs = bytes_ / us / 1e3
+            out.append({"kind": "gemv", "case": name, "N": N, "K": K, "batch": batch, "bytes": bytes_,
+                        "us_per_layer": round(us, 3), "gbs": round(gbs, 1),
+                        "frac_of_measured_hbm": round(gbs / peak, 4), "frac_of_8000": round(gbs / 8000.0, 4),
+                        "sets": r})
+            del sets
+            torch.cuda.empty_cache()
+    for d in out:
+        what = d["case"] + (f" {d['out']}" if d["kind"] == "dequant" else f" B={d['batch']}")
+        t = d["us"] if d["kind"] == "dequant" else d["us_per_layer"]
+        print(f"{d['kind']:8s} {what:44s} {t:10.3f} us {d['gbs']:9.1f} GB/s "
+              f"{100 * d['frac_of_measured_hbm']:5.1f}% of {peak:.0f} ({peak_kind}) "
+              f"{100 * d['frac_of_8000']:5.1f}% of 8000", file=sys.stderr)
+    return {"sweep": out, "peak_gbs": peak, "peak_kind": peak_kind,
+            "timing": "CUDA graph of back-to-back launches over rotating input sets (> 4x L2), "
+                      "events at the graph's ends, best of 5 replays",
+            "data": "synthetic random codes and scales"}
+
+
 def main():
     faulthandler.enable()
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
@@ -465,6 +608,8 @@ def main():
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time every dequant and GEMV configuration instead of the step")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -479,6 +624,10 @@ def main():
         if rank != 0:
             return
         print(json.dumps(run_reference(args)), flush=True)
+        return
+    if args.sweep:
+        if rank == 0:
+            print(json.dumps(run_sweep(args)), flush=True)
         return
 
     if world > 1:
