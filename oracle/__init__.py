@@ -12,7 +12,9 @@ ctypes and numpy.  Each function names the passage it follows:
 * quantization: "NF4反量化算子优化", sections "双量化" (first and second level),
   and the report "NF4 双重量化反量化 CUDA Kernel 实现报告" section 1.2;
 * dequantization: the report, section 1.3 (formula) and 2.2 (nibble order);
-* GEMV: "RTX 4060 上的 LLM 量化实测", section "Fused kernel：把反量化搬到片上".
+* GEMV: "RTX 4060 上的 LLM 量化实测", section "Fused kernel：把反量化搬到片上";
+* the layer's output stage (bias added to the row sum, result stored in the
+  layer's 16-bit type): the same section.
 
 Every function here is pinned by tests under ``tests/`` (``-m "not gpu"``)
 against values and properties the pages and the mathematics fix.
@@ -33,6 +35,7 @@ _lib = None
 
 BF16 = 0
 FP16 = 1
+F32 = 2
 
 
 def build(force: bool = False) -> str:
@@ -79,6 +82,15 @@ def _load():
     lib.oracle_dequant.argtypes = [P, P, P, P, ctypes.c_float, I64, I64, I64, ctypes.c_int, P]
     lib.oracle_dequant_at.argtypes = [P, P, P, P, ctypes.c_float, I64, I64, ctypes.c_int, P, I64, P]
     lib.oracle_gemv.argtypes = [P, P, P, P, ctypes.c_float, I64, I64, I64, I64, P, I64, P, I64, P, P]
+    lib.oracle_f64_to_bf16.argtypes = [ctypes.c_double]
+    lib.oracle_f64_to_bf16.restype = ctypes.c_uint16
+    lib.oracle_f64_to_f32_bits.argtypes = [ctypes.c_double]
+    lib.oracle_f64_to_f32_bits.restype = ctypes.c_uint32
+    lib.oracle_round_f64.argtypes = [ctypes.c_double, ctypes.c_int]
+    lib.oracle_round_f64.restype = ctypes.c_uint32
+    lib.oracle_decode.argtypes = [ctypes.c_uint32, ctypes.c_int]
+    lib.oracle_decode.restype = ctypes.c_double
+    lib.oracle_gemv_output.argtypes = [P, I64, I64, P, P, ctypes.c_int, P, P]
     _lib = lib
     return lib
 
@@ -250,3 +262,48 @@ def gemv(t: NF4Tensor, N: int, K: int, x_bf16: np.ndarray, rows: np.ndarray | No
                         ctypes.c_float(t.offset), N, K, t.blocksize, t.s2_blocksize, _ptr(x), batch,
                         rp, count, _ptr(y), _ptr(s))
     return y, s
+
+
+# --------------------------------------------------------------------------
+# output stage of a layer: bias and the output type
+# ("RTX 4060 上的 LLM 量化实测", section "Fused kernel：把反量化搬到片上")
+
+def f64_to_bf16(v: float) -> int:
+    return int(_load().oracle_f64_to_bf16(float(v)))
+
+
+def f64_to_f32_bits(v: float) -> int:
+    return int(_load().oracle_f64_to_f32_bits(float(v)))
+
+
+def round_f64(v: float, dtype: int) -> int:
+    """Pattern of dtype (BF16, FP16, F32) nearest the binary64 value v, ties to even."""
+    return int(_load().oracle_round_f64(float(v), int(dtype)))
+
+
+def decode(bits: int, dtype: int) -> float:
+    """Exact value of a BF16 / FP16 / F32 pattern."""
+    return float(_load().oracle_decode(int(bits), int(dtype)))
+
+
+def gemv_output(y_ref: np.ndarray, dtype: int, bias_bits: np.ndarray | None = None,
+                rows: np.ndarray | None = None):
+    """v = y_ref + bias (binary64, bias widened exactly) and its nearest dtype pattern.
+
+    y_ref is [batch, count] from ``gemv``; bias_bits is [N] (uint16 for BF16/FP16, uint32 for
+    F32) or None. Returns (v float64 [batch, count], y_bits uint32 [batch, count]).
+    """
+    y_ref = np.ascontiguousarray(y_ref, np.float64)
+    batch, count = y_ref.shape
+    bp = None
+    if bias_bits is not None:
+        bias_bits = np.ascontiguousarray(bias_bits, np.uint32 if dtype == F32 else np.uint16)
+        bp = _ptr(bias_bits)
+    rp = None
+    if rows is not None:
+        rows = np.ascontiguousarray(rows, np.int64)
+        rp = _ptr(rows)
+    v = np.zeros((batch, count), np.float64)
+    yb = np.zeros((batch, count), np.uint32)
+    _load().oracle_gemv_output(_ptr(y_ref), batch, count, rp, bp, int(dtype), _ptr(v), _ptr(yb))
+    return v, yb

@@ -15,7 +15,7 @@
  *              1.3 (dequantization formula), 2.2 (nibble order).
  *   [QTAX]     "RTX 4060 上的 LLM 量化实测：4-bit decode 比 FP16 慢在哪里",
  *              section "Fused kernel：把反量化搬到片上" (fused dequant-GEMV
- *              with fp32 accumulation).
+ *              with fp32 accumulation; fp16 output plus the layer's bias).
  *
  * Build with contraction off (gcc -O2 -ffp-contract=off): every float
  * operation below is one IEEE-754 binary32 or binary64 operation, rounded to
@@ -156,6 +156,32 @@ uint16_t oracle_f64_to_f16(double d) {
   uint64_t m;
   split_f64(d, &neg, &m, &e);
   return (uint16_t)round_to_format(neg, m, e, 11, -14, 15, 5);
+}
+
+/* binary64 -> bfloat16 directly (one rounding). */
+uint16_t oracle_f64_to_bf16(double d) {
+  uint64_t u;
+  memcpy(&u, &d, 8);
+  if ((u & 0x7ff0000000000000ull) == 0x7ff0000000000000ull)
+    return (uint16_t)(((u >> 48) & 0x8000u) | 0x7f80u |
+                      ((u & 0xfffffffffffffull) ? 0x40u : 0u));
+  int neg, e;
+  uint64_t m;
+  split_f64(d, &neg, &m, &e);
+  return (uint16_t)round_to_format(neg, m, e, 8, -126, 127, 8);
+}
+
+/* binary64 -> binary32 bit pattern (one rounding, subnormals kept). */
+uint32_t oracle_f64_to_f32_bits(double d) {
+  uint64_t u;
+  memcpy(&u, &d, 8);
+  if ((u & 0x7ff0000000000000ull) == 0x7ff0000000000000ull)
+    return (uint32_t)(((u >> 32) & 0x80000000u) | 0x7f800000u |
+                      ((u & 0xfffffffffffffull) ? 0x400000u : 0u));
+  int neg, e;
+  uint64_t m;
+  split_f64(d, &neg, &m, &e);
+  return round_to_format(neg, m, e, 24, -126, 127, 8);
 }
 
 /* binary16 -> binary32 (exact). */
@@ -372,6 +398,47 @@ void oracle_gemv(const uint8_t* packed, const uint8_t* absmax_q,
       }
       y_ref[b * count + i] = acc;
       s_abs[b * count + i] = acc_abs;
+    }
+  }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Output stage of a layer ([QTAX], fused kernel section: each binary32 row
+ * sum is stored in the layer's 16-bit type and the layer's bias is added to
+ * the stored row).  Types: 0 bfloat16, 1 binary16, 2 binary32.
+ *   oracle_round_f64: the pattern of `dtype` nearest v (ties to even);
+ *   oracle_decode:    the exact value of a pattern of `dtype`;
+ *   oracle_gemv_output: v[b][i] = y_ref[b][i] + bias[r_i] in binary64, with
+ *     the bias pattern widened exactly (bias == NULL: no bias; rows == NULL:
+ *     r_i = i), and y_bits[b][i] = oracle_round_f64(v[b][i], dtype).        */
+uint32_t oracle_round_f64(double v, int dtype) {
+  if (dtype == 0) return oracle_f64_to_bf16(v);
+  if (dtype == 1) return oracle_f64_to_f16(v);
+  return oracle_f64_to_f32_bits(v);
+}
+
+double oracle_decode(uint32_t bits, int dtype) {
+  if (dtype == 0) return (double)oracle_bf16_to_f32((uint16_t)bits);
+  if (dtype == 1) return (double)oracle_f16_to_f32((uint16_t)bits);
+  float f;
+  memcpy(&f, &bits, 4);
+  return (double)f;
+}
+
+void oracle_gemv_output(const double* y_ref, int64_t batch, int64_t count, const int64_t* rows,
+                        const void* bias, int dtype, double* v, uint32_t* y_bits) {
+  for (int64_t b = 0; b < batch; ++b) {
+    for (int64_t i = 0; i < count; ++i) {
+      const int64_t r = rows ? rows[i] : i;
+      double bv = 0.0;
+      if (bias) {
+        const uint32_t bb = dtype == 2 ? ((const uint32_t*)bias)[r]
+                                       : (uint32_t)((const uint16_t*)bias)[r];
+        bv = oracle_decode(bb, dtype);
+      }
+      const double val = y_ref[b * count + i] + bv;
+      v[b * count + i] = val;
+      y_bits[b * count + i] = oracle_round_f64(val, dtype);
     }
   }
 }

@@ -118,6 +118,19 @@ def activations(seed: int, batch: int, K: int) -> np.ndarray:
     return normal_bf16(seed, batch * K).reshape(batch, K)
 
 
+def bias(seed: int, N: int, dtype: str) -> np.ndarray:
+    """Layer bias ~ N(0, 1) in the output type ("bf16", "fp16" or "f32") as bit
+    patterns: uint16 for the 16-bit types (nearest even), uint32 for binary32."""
+    if dtype == "bf16":
+        return normal_bf16(seed, N)
+    f = normal(seed, N)
+    if dtype == "fp16":
+        return f.astype(np.float16).view(np.uint16)
+    if dtype == "f32":
+        return f.view(np.uint32).copy()
+    raise ValueError(dtype)
+
+
 @dataclass(frozen=True)
 class Layer:
     name: str
