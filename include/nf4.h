@@ -65,13 +65,15 @@ typedef enum {
   NF4_ERR_INVALID_SIZE = 2,          /* negative size, odd K, size overflow */
   NF4_ERR_UNSUPPORTED_BLOCKSIZE = 3, /* blocksize / s2_blocksize not a supported power of two */
   NF4_ERR_MISALIGNED = 4,            /* pointer not aligned to its element size */
-  NF4_ERR_UNSUPPORTED_DTYPE = 5,     /* out_dtype not NF4_BF16 / NF4_FP16 */
+  NF4_ERR_UNSUPPORTED_DTYPE = 5,     /* output type not accepted by the call */
   NF4_ERR_UNSUPPORTED_BATCH = 6,     /* GEMV batch outside 1..8 */
   NF4_ERR_CUDA = 7,                  /* a CUDA runtime call failed */
   NF4_ERR_WORKSPACE = 8              /* workspace missing or too small */
 } nf4_status;
 
-typedef enum { NF4_BF16 = 0, NF4_FP16 = 1 } nf4_dtype;
+/* Output element types: bfloat16, binary16 (IEEE half), binary32. nf4_dequant
+ * writes the two 16-bit types; nf4_gemv_ex writes all three. */
+typedef enum { NF4_BF16 = 0, NF4_FP16 = 1, NF4_F32 = 2 } nf4_dtype;
 
 /* Library version as major*10000 + minor*100 + patch. */
 NF4_API int nf4_version(void);
@@ -147,6 +149,37 @@ NF4_API nf4_status nf4_gemv(const uint8_t* packed, const uint8_t* absmax_q,
                     const uint16_t* absmax2, const uint16_t* code2, float offset,
                     int64_t N, int64_t K, int32_t blocksize, int32_t s2_blocksize,
                     const uint16_t* x, int32_t batch, float* y, nf4_stream_t stream);
+
+/*
+ * nf4_gemv_ex -- nf4_gemv with the layer's output stage fused: an optional
+ * bias and a 16-bit (or binary32) y. "RTX 4060 上的 LLM 量化实测", section
+ * "Fused kernel：把反量化搬到片上", stores each fp32 row sum as binary16 and
+ * then adds the layer's bias; here both happen in the epilogue of the same
+ * kernel, with a single rounding.
+ *
+ *   packed .. batch  as for nf4_gemv.
+ *   bias         NULL, or [N] elements of y_dtype (device), aligned to its
+ *                element size.
+ *   y            [batch][N] elements of y_dtype (device), aligned likewise:
+ *                y[b][r] = round(fp32(sum_b_r + bias[r])), where sum_b_r is
+ *                a binary32 row sum as accurate as nf4_gemv's y (in practice
+ *                the same kernel and order), bias[r] is widened
+ *                exactly to binary32, the addition is one binary32 operation
+ *                and round is round-to-nearest-even into y_dtype (the
+ *                identity for NF4_F32). Without a bias, y = round(sum_b_r).
+ *                So |y - v| is at most 1e-3 * (sum_k |W_hat x| + |bias[r]|)
+ *                + 1e-6 plus half a unit in the last place of y_dtype, with
+ *                v the exact value sum_k W_hat x + bias[r].
+ *   y_dtype      NF4_BF16, NF4_FP16 or NF4_F32. K == 0 writes round(bias),
+ *                or zeros.
+ * nf4_gemv(..., y, stream) is nf4_gemv_ex(..., NULL, y, NF4_F32, stream).
+ * Errors: as nf4_gemv, plus NF4_ERR_UNSUPPORTED_DTYPE.
+ */
+NF4_API nf4_status nf4_gemv_ex(const uint8_t* packed, const uint8_t* absmax_q,
+                       const uint16_t* absmax2, const uint16_t* code2, float offset,
+                       int64_t N, int64_t K, int32_t blocksize, int32_t s2_blocksize,
+                       const uint16_t* x, int32_t batch, const void* bias, void* y,
+                       nf4_dtype y_dtype, nf4_stream_t stream);
 
 /*
  * nf4_quantize_workspace_size -- bytes of device workspace nf4_quantize needs

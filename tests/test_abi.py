@@ -29,7 +29,7 @@ def declared_functions():
 def test_exports_every_declared_symbol(lib):
     names = declared_functions()
     assert set(names) == {"nf4_version", "nf4_status_string", "nf4_last_cuda_error", "nf4_dequant",
-                          "nf4_gemv", "nf4_quantize_workspace_size", "nf4_quantize",
+                          "nf4_gemv", "nf4_gemv_ex", "nf4_quantize_workspace_size", "nf4_quantize",
                           "nf4_device_error_flags", "nf4_quantize_noalloc"}
     for n in names:
         assert hasattr(lib, n), n
@@ -95,6 +95,25 @@ def test_gemv_argument_errors(lib):
     assert gv(lib, packed=0) == ERR_NULL
     assert gv(lib, y=A + 2) == ERR_ALIGN
     assert gv(lib, x=A + 1) == ERR_ALIGN
+
+
+def test_gemv_ex_argument_errors(lib):
+    def gx(N=16, K=64, x=A, y=A, bias=0, dtype=0, batch=1):
+        return lib.nf4_gemv_ex(P(A), P(A), P(A), P(A), 0.0, N, K, 64, 256, P(x), batch, P(bias),
+                               P(y), dtype, None)
+    for d in (3, -1, 7):
+        assert gx(dtype=d) == ERR_DTYPE, d
+    assert gx(N=-1, dtype=3) == ERR_SIZE  # sizes are checked first
+    assert gx(batch=9) == ERR_BATCH
+    assert gx(N=0, y=0, x=0, dtype=2) == OK
+    assert gx(y=0) == ERR_NULL
+    assert gx(x=0, bias=A) == ERR_NULL
+    # y and bias aligned to the output element size (2 bytes, or 4 for binary32)
+    assert gx(y=A + 1, dtype=0) == ERR_ALIGN
+    assert gx(y=A + 2, dtype=2) == ERR_ALIGN
+    assert gx(bias=A + 1, dtype=1) == ERR_ALIGN
+    assert gx(bias=A + 2, dtype=2) == ERR_ALIGN
+    assert gx(x=A + 1, y=A + 2, bias=A + 6, dtype=0) == ERR_ALIGN  # x misaligned
 
 
 def test_quantize_argument_errors_and_workspace_size(lib):

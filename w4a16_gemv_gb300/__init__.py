@@ -14,7 +14,7 @@ from dataclasses import dataclass
 
 import torch
 
-__all__ = ["NF4Error", "NF4Weight", "nf4_dequant", "nf4_gemv", "nf4_quantize",
+__all__ = ["NF4Error", "NF4Weight", "nf4_dequant", "nf4_gemv", "nf4_gemv_ex", "nf4_quantize",
            "nf4_quantize_workspace_size", "nf4_quantize_noalloc", "nf4_version", "nf4_status_string",
            "nf4_device_error_flags", "LIB_PATH"]
 
@@ -35,6 +35,9 @@ _lib.nf4_dequant.argtypes = [_P, _P, _P, _P, ctypes.c_float, _I64, _I32, _I32, _
 _lib.nf4_dequant.restype = ctypes.c_int
 _lib.nf4_gemv.argtypes = [_P, _P, _P, _P, ctypes.c_float, _I64, _I64, _I32, _I32, _P, _I32, _P, _P]
 _lib.nf4_gemv.restype = ctypes.c_int
+_lib.nf4_gemv_ex.argtypes = [_P, _P, _P, _P, ctypes.c_float, _I64, _I64, _I32, _I32, _P, _I32, _P, _P,
+                             ctypes.c_int, _P]
+_lib.nf4_gemv_ex.restype = ctypes.c_int
 _lib.nf4_quantize_workspace_size.argtypes = [_I64, _I32, _I32]
 _lib.nf4_quantize_workspace_size.restype = ctypes.c_size_t
 _lib.nf4_quantize.argtypes = [_P, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
@@ -46,7 +49,9 @@ _lib.nf4_device_error_flags.restype = ctypes.c_int
 
 NF4_BF16 = 0
 NF4_FP16 = 1
+NF4_F32 = 2
 _DTYPES = {torch.bfloat16: NF4_BF16, torch.float16: NF4_FP16}
+_Y_DTYPES = {torch.bfloat16: NF4_BF16, torch.float16: NF4_FP16, torch.float32: NF4_F32}
 
 
 class NF4Error(RuntimeError):
@@ -165,6 +170,34 @@ def nf4_gemv(packed, absmax_q, absmax2, code2, offset: float, N: int, K: int, x:
     return y
 
 
+def nf4_gemv_ex(packed, absmax_q, absmax2, code2, offset: float, N: int, K: int, x: torch.Tensor,
+                bias: torch.Tensor | None = None, y: torch.Tensor | None = None,
+                out_dtype: torch.dtype = torch.bfloat16, blocksize: int = 64,
+                s2_blocksize: int = 256, stream=None) -> torch.Tensor:
+    """y[b, r] = round(fp32(sum_k W_hat[r, k] x[b, k] + bias[r])) in out_dtype (bf16, fp16 or
+    fp32); bias (optional) is [N] of out_dtype. Returns y [batch, N]."""
+    if out_dtype not in _Y_DTYPES:
+        raise TypeError("out_dtype must be torch.bfloat16, torch.float16 or torch.float32")
+    if x.dim() == 1:
+        x = x.view(1, -1)
+    batch = x.shape[0]
+    if x.shape[1] != K:
+        raise ValueError(f"x has {x.shape[1]} columns, expected K={K}")
+    n = N * K
+    nbytes, nb, ng = _sizes(n, blocksize, s2_blocksize) if n > 0 else (0, 0, 0)
+    if y is None:
+        y = torch.empty((batch, N), dtype=out_dtype, device=x.device)
+    st = _lib.nf4_gemv_ex(_ptr(packed, "packed", torch.uint8, nbytes),
+                          _ptr(absmax_q, "absmax_q", torch.uint8, nb),
+                          _ptr(absmax2, "absmax2", torch.float16, ng),
+                          _ptr(code2, "code2", torch.float16, 256), float(offset), int(N), int(K),
+                          int(blocksize), int(s2_blocksize), _ptr(x, "x", torch.bfloat16, batch * K),
+                          int(batch), _ptr(bias, "bias", out_dtype, N),
+                          _ptr(y, "y", out_dtype, batch * N), _Y_DTYPES[out_dtype], _stream(stream))
+    _check(st, "nf4_gemv_ex")
+    return y
+
+
 def nf4_quantize_workspace_size(n: int, blocksize: int = 64, s2_blocksize: int = 256) -> int:
     return int(_lib.nf4_quantize_workspace_size(int(n), int(blocksize), int(s2_blocksize)))
 
@@ -220,7 +253,13 @@ def dequant(wt: NF4Weight, out_dtype: torch.dtype = torch.bfloat16, out=None, st
                        wt.s2_blocksize, out=out, out_dtype=out_dtype, stream=stream)
 
 
-def gemv(wt: NF4Weight, x: torch.Tensor, y=None, stream=None):
+def gemv(wt: NF4Weight, x: torch.Tensor, y=None, stream=None, bias=None, out_dtype=None):
+    """Fused GEMV of an N x K weight: fp32 y by default; with a bias or an out_dtype, the fused
+    output stage of nf4_gemv_ex."""
     N, K = wt.shape
-    return nf4_gemv(wt.packed, wt.absmax_q, wt.absmax2, wt.code2, wt.offset, N, K, x, y=y,
-                    blocksize=wt.blocksize, s2_blocksize=wt.s2_blocksize, stream=stream)
+    if bias is None and out_dtype in (None, torch.float32):
+        return nf4_gemv(wt.packed, wt.absmax_q, wt.absmax2, wt.code2, wt.offset, N, K, x, y=y,
+                        blocksize=wt.blocksize, s2_blocksize=wt.s2_blocksize, stream=stream)
+    return nf4_gemv_ex(wt.packed, wt.absmax_q, wt.absmax2, wt.code2, wt.offset, N, K, x, bias=bias,
+                       y=y, out_dtype=out_dtype or torch.float32, blocksize=wt.blocksize,
+                       s2_blocksize=wt.s2_blocksize, stream=stream)

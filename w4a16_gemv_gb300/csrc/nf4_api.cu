@@ -69,7 +69,9 @@ const char* nf4_status_string(nf4_status status) {
       return "NF4_ERR_UNSUPPORTED_BLOCKSIZE: block sizes must be powers of two "
              "(blocksize 2..2^20, s2_blocksize 1..2^20)";
     case NF4_ERR_MISALIGNED: return "NF4_ERR_MISALIGNED: pointer not aligned to its element size";
-    case NF4_ERR_UNSUPPORTED_DTYPE: return "NF4_ERR_UNSUPPORTED_DTYPE: out_dtype must be NF4_BF16 or NF4_FP16";
+    case NF4_ERR_UNSUPPORTED_DTYPE:
+      return "NF4_ERR_UNSUPPORTED_DTYPE: dequant output must be NF4_BF16 or NF4_FP16, "
+             "GEMV output NF4_BF16, NF4_FP16 or NF4_F32";
     case NF4_ERR_UNSUPPORTED_BATCH: return "NF4_ERR_UNSUPPORTED_BATCH: batch must be 1..8";
     case NF4_ERR_CUDA: return "NF4_ERR_CUDA: a CUDA runtime call failed (see nf4_last_cuda_error)";
     case NF4_ERR_WORKSPACE: return "NF4_ERR_WORKSPACE: workspace missing or too small";
@@ -102,10 +104,11 @@ nf4_status nf4_dequant(const uint8_t* packed, const uint8_t* absmax_q, const uin
   return cuda_status(nf4::launch_dequant(t, n, out, out_dtype, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-nf4_status nf4_gemv(const uint8_t* packed, const uint8_t* absmax_q, const uint16_t* absmax2,
-                    const uint16_t* code2, float offset, int64_t N, int64_t K, int32_t blocksize,
-                    int32_t s2_blocksize, const uint16_t* x, int32_t batch, float* y,
-                    nf4_stream_t stream) {
+nf4_status nf4_gemv_ex(const uint8_t* packed, const uint8_t* absmax_q, const uint16_t* absmax2,
+                       const uint16_t* code2, float offset, int64_t N, int64_t K,
+                       int32_t blocksize, int32_t s2_blocksize, const uint16_t* x,
+                       int32_t batch, const void* bias, void* y, nf4_dtype y_dtype,
+                       nf4_stream_t stream) {
   if (N < 0 || K < 0 || (K & 1) != 0) return NF4_ERR_INVALID_SIZE;
   if (K > 0 && N > kMaxElems / K) return NF4_ERR_INVALID_SIZE;
   if (N > kMaxElems) return NF4_ERR_INVALID_SIZE;
@@ -113,9 +116,12 @@ nf4_status nf4_gemv(const uint8_t* packed, const uint8_t* absmax_q, const uint16
   nf4_status st = check_block_sizes(blocksize, s2_blocksize, &lbs, &ls2);
   if (st != NF4_OK) return st;
   if (batch < 1 || batch > 8) return NF4_ERR_UNSUPPORTED_BATCH;
+  if (y_dtype != NF4_BF16 && y_dtype != NF4_FP16 && y_dtype != NF4_F32)
+    return NF4_ERR_UNSUPPORTED_DTYPE;
   if (N == 0) return NF4_OK;
   if (!y) return NF4_ERR_NULL;
-  if (!aligned(y, 4)) return NF4_ERR_MISALIGNED;
+  const uintptr_t ysize = y_dtype == NF4_F32 ? 4 : 2;
+  if (!aligned(y, ysize) || (bias && !aligned(bias, ysize))) return NF4_ERR_MISALIGNED;
   if (K > 0) {
     st = check_quant_inputs(packed, absmax_q, absmax2, code2);
     if (st != NF4_OK) return st;
@@ -123,8 +129,17 @@ nf4_status nf4_gemv(const uint8_t* packed, const uint8_t* absmax_q, const uint16
     if (!aligned(x, 2)) return NF4_ERR_MISALIGNED;
   }
   const nf4::QuantTensor t{packed, absmax_q, absmax2, code2, offset, lbs, ls2};
+  const nf4::YOut out{y, bias, int(y_dtype)};
   return cuda_status(
-      nf4::launch_gemv(t, N, K, x, batch, y, reinterpret_cast<cudaStream_t>(stream)));
+      nf4::launch_gemv(t, N, K, x, batch, out, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+nf4_status nf4_gemv(const uint8_t* packed, const uint8_t* absmax_q, const uint16_t* absmax2,
+                    const uint16_t* code2, float offset, int64_t N, int64_t K, int32_t blocksize,
+                    int32_t s2_blocksize, const uint16_t* x, int32_t batch, float* y,
+                    nf4_stream_t stream) {
+  return nf4_gemv_ex(packed, absmax_q, absmax2, code2, offset, N, K, blocksize, s2_blocksize, x,
+                     batch, nullptr, y, NF4_F32, stream);
 }
 
 size_t nf4_quantize_workspace_size(int64_t n, int32_t blocksize, int32_t s2_blocksize) {

@@ -112,7 +112,7 @@ __device__ __forceinline__ void build_pair_table(uint32_t* sTab) {
 template <int B, int CB, int R>
 __global__ void __launch_bounds__(kThreads) gemv_fast_kernel(QuantTensor t, int64_t N, int64_t K,
                                                              int ks, const uint16_t* __restrict__ x,
-                                                             float* __restrict__ y) {
+                                                             const YOut y) {
   extern __shared__ __align__(16) uint32_t sTab[];
   __shared__ float sC2[256];
   __shared__ float sRed[kWarps][R * B];
@@ -195,7 +195,8 @@ __global__ void __launch_bounds__(kThreads) gemv_fast_kernel(QuantTensor t, int6
       for (int r = 0; r < R; ++r)
         if (row0 + r < N)
 #pragma unroll
-          for (int b = 0; b < B; ++b) y[int64_t(b) * N + row0 + r] = acc[r][b];
+          for (int b = 0; b < B; ++b)
+            y_store(y, int64_t(b) * N + row0 + r, acc[r][b], y_bias_bits(y, row0 + r));
     }
   } else {
     if (lane == 0) {
@@ -209,7 +210,7 @@ __global__ void __launch_bounds__(kThreads) gemv_fast_kernel(QuantTensor t, int6
       float v = 0.0f;
       for (int j = 0; j < ks; ++j) v += sRed[warp + j][lane];
       const int r = lane / B, b = lane - (lane / B) * B;
-      if (row0 + r < N) y[int64_t(b) * N + row0 + r] = v;
+      if (row0 + r < N) y_store(y, int64_t(b) * N + row0 + r, v, y_bias_bits(y, row0 + r));
     }
   }
 }
@@ -220,7 +221,7 @@ template <int B>
 __global__ void __launch_bounds__(kThreads) gemv_generic_kernel(QuantTensor t, int64_t N,
                                                                 int64_t K,
                                                                 const uint16_t* __restrict__ x,
-                                                                float* __restrict__ y) {
+                                                                const YOut y) {
   __shared__ float sT[16];
   __shared__ float sC2[256];
   pdl_allow_dependents();
@@ -252,7 +253,7 @@ __global__ void __launch_bounds__(kThreads) gemv_generic_kernel(QuantTensor t, i
 #pragma unroll
     for (int b = 0; b < B; ++b) {
       const float v = warp_sum(acc[b]);
-      if (lane == 0) y[int64_t(b) * N + row] = v;
+      if (lane == 0) y_store(y, int64_t(b) * N + row, v, y_bias_bits(y, row));
     }
   }
 }
@@ -269,7 +270,7 @@ struct FastConfig {
 
 template <int B, int CB, int R>
 cudaError_t launch_fast_typed(const QuantTensor& t, int64_t N, int64_t K, int ks,
-                              const uint16_t* x, float* y, cudaStream_t stream) {
+                              const uint16_t* x, const YOut& y, cudaStream_t stream) {
   static_assert(kTableBytes <= 48 * 1024, "table fits the default dynamic shared memory");
   const int64_t rows_per_cta = int64_t(kWarps / ks) * R;
   const int64_t blocks = (N + rows_per_cta - 1) / rows_per_cta;
@@ -277,18 +278,18 @@ cudaError_t launch_fast_typed(const QuantTensor& t, int64_t N, int64_t K, int ks
                   stream, t, N, K, ks, x, y);
 }
 
-// K == 0: every output is an empty sum.
-__global__ void zero_fill_kernel(float* __restrict__ y, int64_t count) {
+// K == 0: every output is an empty sum (plus the bias, if any).
+__global__ void zero_fill_kernel(const YOut y, int64_t N, int64_t count) {
   pdl_allow_dependents();
   pdl_wait_prior_grid();
   for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < count;
        i += int64_t(gridDim.x) * blockDim.x)
-    y[i] = 0.0f;
+    y_store(y, i, 0.0f, y_bias_bits(y, i % N));
 }
 
 template <int B>
 cudaError_t launch_generic_typed(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x,
-                                 float* y, cudaStream_t stream) {
+                                 const YOut& y, cudaStream_t stream) {
   const int sms = device_sm_count();
   int64_t blocks = (N + kWarps - 1) / kWarps;
   const int64_t max_blocks = int64_t(sms > 0 ? sms : 1) * 8;
@@ -345,14 +346,14 @@ FastConfig choose_config(const QuantTensor& t, int64_t N, int64_t K, int batch,
 
 template <int B>
 cudaError_t dispatch_batch(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x,
-                           float* y, cudaStream_t stream) {
+                           const YOut& y, cudaStream_t stream) {
   const int sms = device_sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   if (K == 0) {
     const int64_t count = int64_t(B) * N;
     int64_t blocks = (count + kThreads - 1) / kThreads;
     if (blocks > int64_t(sms) * 8) blocks = int64_t(sms) * 8;
-    return launch_k(zero_fill_kernel, dim3(unsigned(blocks)), dim3(kThreads), 0, stream, y, count);
+    return launch_k(zero_fill_kernel, dim3(unsigned(blocks)), dim3(kThreads), 0, stream, y, N, count);
   }
   {
     bool done = false;
@@ -403,7 +404,7 @@ cudaError_t read_and_clear_device_flags(unsigned int* flags) {
 }
 
 cudaError_t launch_gemv(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x, int batch,
-                        float* y, cudaStream_t stream) {
+                        const YOut& y, cudaStream_t stream) {
   switch (batch) {
     case 1: return dispatch_batch<1>(t, N, K, x, y, stream);
     case 2: return dispatch_batch<2>(t, N, K, x, y, stream);

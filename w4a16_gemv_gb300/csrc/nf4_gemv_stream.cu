@@ -57,7 +57,7 @@ constexpr int kMaxSmemPerCta = 227 * 1024;
 struct B1Args {
   QuantTensor t;
   const uint16_t* x;
-  float* y;
+  YOut out;
   int64_t N;
   int32_t K;
   int grid;  // CTAs; CTA b owns rows [b*N/grid, (b+1)*N/grid)
@@ -65,7 +65,7 @@ struct B1Args {
   int G;     // row groups
   int spr;   // quantization blocks per row
   int cpr;   // column chunks per row
-  uint32_t off_c2, off_a2, off_xs, off_q, off_scale, off_part, off_tab;
+  uint32_t off_c2, off_a2, off_xs, off_q, off_scale, off_part, off_bias, off_tab;
 };
 
 struct B1Plan {
@@ -99,6 +99,16 @@ __device__ __forceinline__ uint16_t ldg_u16_ordered(const uint16_t* p) {
   unsigned short v;
   asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
   return v;
+}
+__device__ __forceinline__ uint32_t ldg_u32_ordered(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+// Bias bits of row r (16 or 32 bits as stored), issued in program order.
+__device__ __forceinline__ uint32_t bias_bits_ordered(const YOut& o, int64_t r) {
+  if (o.dtype == NF4_F32) return ldg_u32_ordered(reinterpret_cast<const uint32_t*>(o.bias) + r);
+  return ldg_u16_ordered(reinterpret_cast<const uint16_t*>(o.bias) + r);
 }
 __device__ __forceinline__ uint8_t ldg_u8_ordered(const uint8_t* p) {
   unsigned int v;
@@ -338,6 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_b1_kernel(const B1Args p) {
   unsigned char* sQ = smem + p.off_q;
   float* sScale = reinterpret_cast<float*>(smem + p.off_scale);
   float* sPart = reinterpret_cast<float*>(smem + p.off_part);
+  uint32_t* sBias = reinterpret_cast<uint32_t*>(smem + p.off_bias);
 
   const int64_t row_bytes = K >> 1;
   const int64_t row_begin = (int64_t(blockIdx.x) * N) / p.grid;
@@ -402,6 +413,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_b1_kernel(const B1Args p) {
   if (tid < q_head) qi = tid;
   else if (tid >= 32 && tid - 32 < nq - q_mid_end) qi = q_mid_end + (tid - 32);
   const uint8_t qb = qi >= 0 ? ldg_u8_ordered(t.absmax_q + b0 + qi) : uint8_t(0);
+  // bias of the CTA's rows, kept (as stored) in shared memory for the end
+  const bool has_bias = p.out.bias != nullptr;
+  const uint32_t bias_v = (has_bias && tid < nrows) ? bias_bits_ordered(p.out, row_begin + tid) : 0u;
   // Shared copies of the small inputs (further batches for long ranges).
   if (tid < 256) sC2[tid] = half_bits_to_float(c2v);
 #pragma unroll
@@ -411,6 +425,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_b1_kernel(const B1Args p) {
     if (i < q_vecs) *reinterpret_cast<uint4*>(sQ + q_lead + q_head + 16 * i) = qm[j];
   }
   if (qi >= 0) sQ[q_lead + qi] = qb;
+  if (has_bias) {
+    if (tid < nrows) sBias[tid] = bias_v;
+    for (int i = tid + kThreads; i < nrows; i += kThreads) sBias[i] = y_bias_bits(p.out, row_begin + i);
+  }
   for (int base = 4 * kThreads; base < ng; base += 4 * kThreads) {  // small group sizes only
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -538,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_b1_kernel(const B1Args p) {
   for (int r = rg0 + gt; r < rg1; r += p.W * 32) {
     float v = 0.0f;
     for (int w = 0; w < p.W; ++w) v += sPart[r * p.W + w];
-    p.y[row_begin + r] = v;
+    y_store(p.out, row_begin + r, v, has_bias ? sBias[r] : 0u);
   }
 }
 
@@ -559,8 +577,8 @@ int reserved_smem_per_block() {
 // sums] below the pair table (+ binary16 x) at shared window address 64 KB.
 // The dynamic window starts after the per-block reserved shared memory (the
 // kernel has no static shared variables).
-bool plan_b1(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x, float* y, int cb,
-             int threads, int sms, B1Plan* plan) {
+bool plan_b1(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x, const YOut& out,
+             int cb, int threads, int sms, B1Plan* plan) {
   const int kWarps = threads / 32;
   B1Args* p = &plan->a;
   const int64_t bs = int64_t(1) << t.lbs;
@@ -573,7 +591,7 @@ bool plan_b1(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x, floa
   if (G > kMaxGroups) G = kMaxGroups;
   p->t = t;
   p->x = x;
-  p->y = y;
+  p->out = out;
   p->N = N;
   p->K = int32_t(K);
   p->W = W;
@@ -601,6 +619,8 @@ bool plan_b1(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x, floa
   off += align_up_u32(uint32_t(max_nq * 4), 128);
   p->off_part = off;
   off += align_up_u32(uint32_t(max_rows * W * 4), 128);
+  p->off_bias = off;
+  if (out.bias) off += align_up_u32(uint32_t(max_rows * 4), 128);
   const uint32_t tab = 65536u - uint32_t(res);
   if (off > tab) return false;
   p->off_tab = tab;
@@ -725,7 +745,7 @@ __device__ __forceinline__ void consume_n(const uint8_t* lane_src, uint32_t row_
 struct BNArgs {
   QuantTensor t;
   const uint16_t* x;
-  float* y;
+  YOut out;
   int64_t N;
   int32_t K;
   int batch;   // real vectors (<= BP)
@@ -735,7 +755,7 @@ struct BNArgs {
   int spr;     // quantization blocks per row
   int cpr;     // column chunks per row
   int slices;  // column slices of W * 32 chunks
-  uint32_t off_c2, off_a2, off_q, off_scale, off_part, off_tab;
+  uint32_t off_c2, off_a2, off_q, off_scale, off_part, off_bias, off_tab;
 };
 
 template <int BP, int CB, int RPG>
@@ -771,6 +791,7 @@ __global__ void __launch_bounds__(512, 1) gemv_bn_kernel(const BNArgs p) {
   unsigned char* sQ = smem + p.off_q;
   float* sScale = reinterpret_cast<float*>(smem + p.off_scale);
   float* sPart = reinterpret_cast<float*>(smem + p.off_part);
+  uint32_t* sBias = reinterpret_cast<uint32_t*>(smem + p.off_bias);
 
   const int64_t row_bytes = K >> 1;
   const int64_t row_begin = (int64_t(blockIdx.x) * N) / p.grid;
@@ -817,6 +838,9 @@ __global__ void __launch_bounds__(512, 1) gemv_bn_kernel(const BNArgs p) {
   if (tid < q_head) qi = tid;
   else if (tid >= 32 && tid - 32 < nq - q_mid_end) qi = q_mid_end + (tid - 32);
   const uint8_t qb = qi >= 0 ? ldg_u8_ordered(t.absmax_q + b0 + qi) : uint8_t(0);
+  // bias of the CTA's rows, kept (as stored) in shared memory for the end
+  const bool has_bias = p.out.bias != nullptr;
+  const uint32_t bias_v = (has_bias && tid < nrows) ? bias_bits_ordered(p.out, row_begin + tid) : 0u;
   if (tid < 256) sC2[tid] = half_bits_to_float(c2v);
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
@@ -825,6 +849,10 @@ __global__ void __launch_bounds__(512, 1) gemv_bn_kernel(const BNArgs p) {
     if (i < q_vecs) *reinterpret_cast<uint4*>(sQ + q_lead + q_head + 16 * i) = qm[j];
   }
   if (qi >= 0) sQ[q_lead + qi] = qb;
+  if (has_bias) {
+    if (tid < nrows) sBias[tid] = bias_v;
+    for (int i = tid + kThreads; i < nrows; i += kThreads) sBias[i] = y_bias_bits(p.out, row_begin + i);
+  }
   for (int base = 4 * kThreads; base < ng; base += 4 * kThreads) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -889,13 +917,13 @@ __global__ void __launch_bounds__(512, 1) gemv_bn_kernel(const BNArgs p) {
     if (b >= p.batch) continue;
     float v = 0.0f;
     for (int w = 0; w < p.W; ++w) v += sPart[(r * BP + b) * p.W + w];
-    p.y[int64_t(b) * N + row_begin + r] = v;
+    y_store(p.out, int64_t(b) * N + row_begin + r, v, has_bias ? sBias[r] : 0u);
   }
 }
 
 // Plan for BP vectors and CB-byte chunks (512 threads, one CTA per SM).
-bool plan_bn(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x, int batch, float* y,
-             int bp, int cb, int sms, BNArgs* p, uint32_t* smem_bytes) {
+bool plan_bn(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x, int batch,
+             const YOut& out, int bp, int cb, int sms, BNArgs* p, uint32_t* smem_bytes) {
   const int64_t bs = int64_t(1) << t.lbs;
   const int ce = 2 * cb;
   if (N <= 0 || K % 32 != 0 || K % bs != 0 || bs < ce) return false;
@@ -910,7 +938,7 @@ bool plan_bn(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x, int 
   if (G > kMaxGroups) G = kMaxGroups;
   p->t = t;
   p->x = x;
-  p->y = y;
+  p->out = out;
   p->N = N;
   p->K = int32_t(K);
   p->batch = batch;
@@ -939,6 +967,8 @@ bool plan_bn(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x, int 
   off += align_up_u32(uint32_t(max_nq * 4), 128);
   p->off_part = off;
   off += align_up_u32(uint32_t(max_rows * bp * W * 4), 128);
+  p->off_bias = off;
+  if (out.bias) off += align_up_u32(uint32_t(max_rows * 4), 128);
   const uint32_t tab = 65536u - uint32_t(res);
   if (off > tab) return false;
   p->off_tab = tab;
@@ -964,8 +994,8 @@ cudaError_t launch_bn(const BNArgs& a, uint32_t smem_bytes, cudaStream_t stream)
 
 }  // namespace
 
-cudaError_t try_gemv_b1(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x, float* y,
-                        int sms, cudaStream_t stream, bool* done) {
+cudaError_t try_gemv_b1(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x,
+                        const YOut& y, int sms, cudaStream_t stream, bool* done) {
   *done = false;
   if ((reinterpret_cast<uintptr_t>(t.packed) & 15u) != 0 || (reinterpret_cast<uintptr_t>(x) & 15u) != 0)
     return cudaSuccess;
@@ -987,7 +1017,7 @@ cudaError_t try_gemv_b1(const QuantTensor& t, int64_t N, int64_t K, const uint16
 }
 
 cudaError_t try_gemv_bn(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x, int batch,
-                        float* y, int sms, cudaStream_t stream, bool* done) {
+                        const YOut& y, int sms, cudaStream_t stream, bool* done) {
   *done = false;
   if (batch < 2 || batch > 8) return cudaSuccess;
   if ((reinterpret_cast<uintptr_t>(t.packed) & 15u) != 0 || (reinterpret_cast<uintptr_t>(x) & 15u) != 0)

@@ -52,6 +52,40 @@ __device__ __forceinline__ float half_bits_to_float(uint16_t h) {
   return __half2float(__ushort_as_half(h));
 }
 
+// Where a GEMV writes its result. Element (b, r) of y is
+// round_dtype(fp32(sum + bias[r])): the binary32 sum, plus the bias widened
+// exactly to binary32 (one rounded addition), then one rounding to nearest
+// even into the output type. Without a bias the sum is rounded directly.
+struct YOut {
+  void* y;           // [batch][N] of dtype
+  const void* bias;  // [N] of dtype, or nullptr
+  int dtype;         // NF4_BF16, NF4_FP16 or NF4_F32
+};
+
+// Bias bits of row r as stored (16 or 32 bits), 0 without a bias.
+__device__ __forceinline__ uint32_t y_bias_bits(const YOut& o, int64_t r) {
+  if (!o.bias) return 0u;
+  if (o.dtype == NF4_F32) return __ldg(reinterpret_cast<const uint32_t*>(o.bias) + r);
+  return __ldg(reinterpret_cast<const uint16_t*>(o.bias) + r);
+}
+
+// Stores element idx of y from the binary32 sum and the row's bias bits.
+__device__ __forceinline__ void y_store(const YOut& o, int64_t idx, float sum, uint32_t bias_bits) {
+  float v = sum;
+  if (o.bias) {
+    const float bf = o.dtype == NF4_F32   ? __uint_as_float(bias_bits)
+                     : o.dtype == NF4_BF16 ? __uint_as_float(bias_bits << 16)
+                                           : half_bits_to_float(uint16_t(bias_bits));
+    v = __fadd_rn(v, bf);
+  }
+  if (o.dtype == NF4_F32)
+    reinterpret_cast<float*>(o.y)[idx] = v;
+  else if (o.dtype == NF4_BF16)
+    reinterpret_cast<__nv_bfloat16*>(o.y)[idx] = __float2bfloat16_rn(v);
+  else
+    reinterpret_cast<__half*>(o.y)[idx] = __float2half_rn(v);
+}
+
 // Decoded scale of block b: fp32(fp32(code2[q] * absmax2[g]) + offset), two
 // separately rounded operations (no contraction). `code2f` is the table
 // already widened to binary32 (exact).
@@ -83,7 +117,7 @@ int device_sm_count();
 cudaError_t launch_dequant(const QuantTensor& t, int64_t n, void* out, nf4_dtype dtype,
                            cudaStream_t stream);
 cudaError_t launch_gemv(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x,
-                        int batch, float* y, cudaStream_t stream);
+                        int batch, const YOut& out, cudaStream_t stream);
 size_t quantize_workspace_bytes(int64_t n, int lbs, int ls2);
 cudaError_t launch_quantize(const float* w, int64_t n, int lbs, int ls2, const uint16_t* code2,
                             uint8_t* packed, uint8_t* absmax_q, uint16_t* absmax2,
@@ -175,11 +209,11 @@ cudaError_t read_and_clear_b1_flags(unsigned int* flags);
 
 // Batch-1 GEMV (k-stationary, bulk-copy pipelined). Sets *done when it
 // handled the call; otherwise the caller uses the general kernels.
-cudaError_t try_gemv_b1(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x, float* y,
-                        int sms, cudaStream_t stream, bool* done);
+cudaError_t try_gemv_b1(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x,
+                        const YOut& out, int sms, cudaStream_t stream, bool* done);
 // Batch 2..8 GEMV (k-stationary, binary32 x in registers, column slices).
 cudaError_t try_gemv_bn(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x, int batch,
-                        float* y, int sms, cudaStream_t stream, bool* done);
+                        const YOut& out, int sms, cudaStream_t stream, bool* done);
 
 }  // namespace nf4
 
