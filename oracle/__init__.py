@@ -91,6 +91,7 @@ def _load():
     lib.oracle_decode.argtypes = [ctypes.c_uint32, ctypes.c_int]
     lib.oracle_decode.restype = ctypes.c_double
     lib.oracle_gemv_output.argtypes = [P, I64, I64, P, P, ctypes.c_int, P, P]
+    lib.oracle_gemv_abs.argtypes = [P, P, P, P, ctypes.c_float, I64, I64, I64, I64, P, I64, P]
     _lib = lib
     return lib
 
@@ -307,3 +308,16 @@ def gemv_output(y_ref: np.ndarray, dtype: int, bias_bits: np.ndarray | None = No
     yb = np.zeros((batch, count), np.uint32)
     _load().oracle_gemv_output(_ptr(y_ref), batch, count, rp, bp, int(dtype), _ptr(v), _ptr(yb))
     return v, yb
+
+
+def gemv_abs(t: NF4Tensor, N: int, K: int, e: np.ndarray) -> np.ndarray:
+    """a[b, r] = sum_k |W_hat[r, k]| * e[b, k] (binary64) for e >= 0 [batch, K]: how far a
+    perturbation of the input by at most e moves W_hat x."""
+    assert N * K <= t.n
+    e = np.ascontiguousarray(e, np.float64).reshape(-1, K)
+    batch = e.shape[0]
+    a = np.zeros((batch, N), np.float64)
+    _load().oracle_gemv_abs(_ptr(t.packed), _ptr(t.absmax_q), _ptr(t.absmax2), _ptr(t.code2),
+                            ctypes.c_float(t.offset), N, K, t.blocksize, t.s2_blocksize, _ptr(e),
+                            batch, _ptr(a))
+    return a

@@ -402,6 +402,28 @@ void oracle_gemv(const uint8_t* packed, const uint8_t* absmax_q,
   }
 }
 
+/* Magnitude GEMV for error bounds through chained layers:
+ *   a[b][r] = sum_k |w_hat[r][k]| * e[b][k]   in binary64, e >= 0 given in
+ * binary64 [batch][K]; outputs [batch][N].  A perturbation of the input by
+ * at most e (elementwise) moves the exact product W_hat x by at most a.     */
+void oracle_gemv_abs(const uint8_t* packed, const uint8_t* absmax_q,
+                     const uint16_t* absmax2, const uint16_t* code2, float offset,
+                     int64_t N, int64_t K, int64_t bs, int64_t s2, const double* e,
+                     int64_t batch, double* a) {
+  for (int64_t r = 0; r < N; ++r) {
+    for (int64_t b = 0; b < batch; ++b) {
+      double acc = 0.0;
+      for (int64_t k = 0; k < K; ++k) {
+        const int64_t flat = r * K + k;
+        const float s = oracle_block_scale(absmax_q, absmax2, code2, offset, flat / bs, s2);
+        const float w_hat = NF4_CODE[nibble_at(packed, flat)] * s;
+        acc += fabs((double)w_hat) * e[b * K + k];
+      }
+      a[b * N + r] = acc;
+    }
+  }
+}
+
 /* ------------------------------------------------------------------------ */
 /* Output stage of a layer ([QTAX], fused kernel section: each binary32 row
  * sum is stored in the layer's 16-bit type and the layer's bias is added to

@@ -288,6 +288,20 @@ def test_gemv_matches_numpy_float64_matmul(N, K, batch):
     assert np.all(s >= np.abs(y) * (1 - 1e-15))
 
 
+@pytest.mark.parametrize("N,K,batch", [(7, 128, 1), (5, 192, 3), (3, 70, 2)])
+def test_gemv_abs_matches_numpy_float64_matmul(N, K, batch):
+    t, _ = _gemv_case(N, K, batch, 40 + N)
+    e = np.random.default_rng(N).random((batch, K)) * 10.0 ** np.random.default_rng(K).integers(-6, 2, K)
+    a = oracle.gemv_abs(t, N, K, e)
+    W = np.abs(oracle.dequant_f32(t).astype(np.float64).reshape(N, K))
+    np.testing.assert_allclose(a, e @ W.T, rtol=1e-13, atol=0)
+    # one-hot e picks |column j| exactly
+    for j in (0, K - 1):
+        oh = np.zeros((1, K))
+        oh[0, j] = 1.0
+        np.testing.assert_array_equal(oracle.gemv_abs(t, N, K, oh)[0], W[:, j])
+
+
 def test_gemv_special_cases():
     N, K = 6, 256
     # every block scale is 0.25 * 1 + 0.5 = 0.75: w_hat = fp32(code * 0.75)
