@@ -182,6 +182,67 @@ NF4_API nf4_status nf4_gemv_ex(const uint8_t* packed, const uint8_t* absmax_q,
                        nf4_dtype y_dtype, nf4_stream_t stream);
 
 /*
+ * Decode step: a fixed sequence of fused GEMV nodes (the linear layers of a
+ * decoder's token step), recorded once into a CUDA graph and replayed once
+ * per token. "RTX 4060 上的 LLM 量化实测", sections "逐层 profiling：问题出在哪"
+ * and "为什么是 k/v projection", finds fixed per-call costs dominating the
+ * thin k_proj / v_proj GEMVs of a decode step; a replay pays no host launch
+ * cost, and consecutive kernels overlap their start with the previous
+ * kernel's end (programmatic dependent launch). Work between the GEMVs of a
+ * real decoder (attention, norms, activation) is not part of a step.
+ *
+ * A node is one nf4_gemv_ex call. Its input is the step's x (input = -1) or
+ * the y of an earlier node j (input = j < this node's index), which must be
+ * NF4_BF16 with N_j == K. Node i runs after node i-1 (stream order).
+ */
+typedef struct nf4_gemv_node {
+  const uint8_t* packed;    /* the quantized N x K weight, as for nf4_gemv */
+  const uint8_t* absmax_q;
+  const uint16_t* absmax2;
+  const uint16_t* code2;
+  float offset;
+  int64_t N, K;
+  int32_t blocksize, s2_blocksize;
+  const void* bias;         /* NULL or [N] of y_dtype */
+  int32_t input;            /* -1: the step's x; j >= 0: y of node j */
+  void* y;                  /* [batch][N] of y_dtype, caller-owned */
+  nf4_dtype y_dtype;
+} nf4_gemv_node;
+
+typedef struct nf4_step_st* nf4_step_t;
+
+/*
+ * nf4_step_create -- validate the nodes (each as nf4_gemv_ex would, plus the
+ * input rules above) and record them into a CUDA graph on the current
+ * device. All pointers (weights, x [batch][K], biases, every y) are device
+ * pointers captured by value: they must stay valid, and their contents are
+ * read / written at each nf4_step_launch, not at creation. Nothing is
+ * launched here. The step owns only host-side graph objects (the library
+ * allocates no device buffers); free them with nf4_step_destroy.
+ * Errors: NF4_ERR_NULL (step, nodes, or a node's pointers),
+ *   NF4_ERR_INVALID_SIZE (n_nodes < 1, a bad input index, K != N of the
+ *   input node, or a node's sizes), NF4_ERR_UNSUPPORTED_DTYPE (an input node
+ *   whose y is not NF4_BF16, or a bad y_dtype), the other nf4_gemv_ex errors,
+ *   NF4_ERR_CUDA (stream capture or graph instantiation failed). On error
+ *   *step is NULL.
+ */
+NF4_API nf4_status nf4_step_create(const nf4_gemv_node* nodes, int32_t n_nodes,
+                                   const uint16_t* x, int32_t batch, nf4_step_t* step);
+
+/*
+ * nf4_step_launch -- enqueue one replay of the step on `stream` (returns
+ * without synchronising). Replays on one stream run one after another; two
+ * replays of the same step must not overlap in time (they share every
+ * buffer). Errors: NF4_ERR_NULL, NF4_ERR_CUDA (also when the current device
+ * is not the one the step was created on).
+ */
+NF4_API nf4_status nf4_step_launch(nf4_step_t step, nf4_stream_t stream);
+
+/* nf4_step_destroy -- free a step (NULL is a no-op). Synchronises nothing:
+ * the caller waits for replays in flight first. */
+NF4_API nf4_status nf4_step_destroy(nf4_step_t step);
+
+/*
  * nf4_quantize_workspace_size -- bytes of device workspace nf4_quantize needs
  * for n elements (0 for n <= 0 or unsupported block sizes).
  */

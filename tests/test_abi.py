@@ -30,7 +30,8 @@ def test_exports_every_declared_symbol(lib):
     names = declared_functions()
     assert set(names) == {"nf4_version", "nf4_status_string", "nf4_last_cuda_error", "nf4_dequant",
                           "nf4_gemv", "nf4_gemv_ex", "nf4_quantize_workspace_size", "nf4_quantize",
-                          "nf4_device_error_flags", "nf4_quantize_noalloc"}
+                          "nf4_device_error_flags", "nf4_quantize_noalloc", "nf4_step_create",
+                          "nf4_step_launch", "nf4_step_destroy"}
     for n in names:
         assert hasattr(lib, n), n
 
@@ -157,3 +158,59 @@ def test_quantize_noalloc_argument_errors_and_limit(lib):
     # too large for the fixed scratch: rejected on the host before any CUDA call
     assert q(n=(1 << 28) + 1) == ERR_WS
     assert q(n=1 << 30, bs=2, s2=1) == ERR_WS
+
+
+def test_gemv_node_layout_matches_the_header(tmp_path):
+    """The binding's nf4_gemv_node mirrors the C struct (offsets from a C
+    program compiled against include/nf4.h)."""
+    import shutil
+    import subprocess
+    import w4a16_gemv_gb300 as nf4
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    fields = [f[0] for f in nf4._GemvNode._fields_]
+    src = tmp_path / "layout.c"
+    body = " ".join(f'printf("%zu ", offsetof(nf4_gemv_node, {f}));' for f in fields)
+    src.write_text("#include <stdio.h>\n#include <stddef.h>\n#include \"nf4.h\"\n"
+                   f"int main(void) {{ {body} printf(\"%zu\\n\", sizeof(nf4_gemv_node)); return 0; }}\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True,
+                                          check=True).stdout.split()]
+    want = [getattr(nf4._GemvNode, f).offset for f in fields] + [ctypes.sizeof(nf4._GemvNode)]
+    assert got == want
+
+
+def test_step_argument_errors(lib):
+    """nf4_step_create validates every node on the host before any CUDA call."""
+    import w4a16_gemv_gb300 as nf4
+    Node = nf4._GemvNode
+
+    def node(N=32, K=64, inp=-1, y=A, dtype=0, bias=0):
+        return Node(A, A, A, A, 0.0, N, K, 64, 256, bias or None, inp, y or None, dtype)
+
+    def create(nodes, x=A, batch=1, n=None):
+        arr = (Node * max(len(nodes), 1))(*nodes)
+        h = P()
+        st = lib.nf4_step_create(arr if nodes else None, len(nodes) if n is None else n,
+                                 P(x), batch, ctypes.byref(h))
+        assert h.value is None
+        return st
+    assert lib.nf4_step_create(None, 1, P(A), 1, None) == ERR_NULL
+    assert create([], n=0) == ERR_SIZE
+    assert create([], n=2) == ERR_NULL
+    assert create([node(inp=0)]) == ERR_SIZE              # its own output
+    assert create([node(inp=-2)]) == ERR_SIZE
+    assert create([node(), node(inp=2)]) == ERR_SIZE      # a later node
+    assert create([node(dtype=1), node(K=32, inp=0)]) == ERR_DTYPE  # input must be bf16
+    assert create([node(N=48), node(K=64, inp=0)]) == ERR_SIZE      # K != N of the input
+    assert create([node(), node(K=32, inp=0, y=0)]) == ERR_NULL
+    assert create([node(), node(K=32, inp=0, dtype=5)]) == ERR_DTYPE
+    assert create([node()], batch=9) == ERR_BATCH
+    assert create([node()], x=0) == ERR_NULL
+    assert create([node(y=A + 1)]) == ERR_ALIGN
+    assert create([node(K=63)]) == ERR_SIZE
+    assert lib.nf4_step_launch(None, None) == ERR_NULL
+    assert lib.nf4_step_destroy(None) == OK
+

@@ -1,0 +1,168 @@
+"""GPU tests of the decode step (nf4_step_create / nf4_step_launch): a
+recorded sequence of fused GEMVs, each node's input the step's x or an
+earlier node's bf16 output.
+
+* Parity: a chain of layers against the oracle, with an error bound carried
+  through the chain (each layer's tolerance plus how far its input may be
+  from the oracle's input); every intermediate output is checked.
+* Mechanism: replays write exactly what the same nodes launched one by one
+  write, for new inputs written between replays.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_helpers import decode_bits, dev, to_device, u16_to_torch
+
+pytestmark = pytest.mark.gpu
+
+BF16, FP16, F32 = oracle.BF16, oracle.FP16, oracle.F32
+_TDT = {BF16: torch.bfloat16, FP16: torch.float16, F32: torch.float32}
+
+
+def _weight(t: oracle.NF4Tensor, N: int, K: int):
+    import w4a16_gemv_gb300 as nf4
+    d = to_device(t)
+    return nf4.NF4Weight(d["packed"], d["absmax_q"], d["absmax2"], d["code2"], t.offset, t.n,
+                         (N, K), t.blocksize, t.s2_blocksize)
+
+
+def _bits(y: torch.Tensor) -> np.ndarray:
+    if y.dtype == torch.float32:
+        return y.cpu().numpy().view(np.uint32)
+    return y.view(torch.int16).cpu().numpy().view(np.uint16).astype(np.uint32)
+
+
+def _round_all(v: np.ndarray, dtype: int) -> np.ndarray:
+    return np.vectorize(lambda a: oracle.round_f64(a, dtype), otypes=[np.uint32])(v)
+
+
+# (N, K, y dtype, bias) of a chain: q_proj -> o_proj -> gate_proj -> down_proj
+# shapes of a Qwen2.5-1.5B-sized decoder layer, each feeding the next.
+CHAIN = [(1536, 1536, BF16, True), (1536, 1536, BF16, False), (8960, 1536, BF16, True),
+         (1536, 8960, F32, True)]
+
+
+@pytest.mark.parametrize("batch", [1, 4])
+def test_chain_parity_with_carried_error_bound(batch):
+    import w4a16_gemv_gb300 as nf4
+    ts, nodes, biases = [], [], []
+    for i, (N, K, dt, has_bias) in enumerate(CHAIN):
+        t = oracle.quantize(synth.weights(200 + i, N * K), 64, 256, synth.code2_linear())
+        ts.append(t)
+        name = {BF16: "bf16", FP16: "fp16", F32: "f32"}[dt]
+        b = synth.bias(210 + i, N, name) if has_bias else None
+        biases.append(b)
+        bt = None
+        if b is not None:
+            bt = torch.from_numpy(b.view(np.int32 if dt == F32 else np.int16)).to(dev()).view(_TDT[dt])
+        y = torch.empty((batch, N), dtype=_TDT[dt], device=dev())
+        nodes.append(dict(weight=_weight(t, N, K), y=y, bias=bt, input=i - 1))
+    x_bits = synth.activations(220 + batch, batch, CHAIN[0][1])
+    x = u16_to_torch(x_bits, torch.bfloat16).view(batch, -1)
+    step = nf4.DecodeStep(nodes, x)
+    step.launch()
+    torch.cuda.synchronize()
+
+    x_or = x_bits                              # the oracle's input to the current layer
+    e = np.zeros((batch, CHAIN[0][1]))         # how far the GPU's input may be from it
+    for i, (N, K, dt, _) in enumerate(CHAIN):
+        y_ref, s_abs = oracle.gemv(ts[i], N, K, x_or)
+        p = oracle.gemv_abs(ts[i], N, K, e)
+        v, y_or = oracle.gemv_output(y_ref, dt, biases[i])
+        babs = 0.0 if biases[i] is None else np.abs(decode_bits(biases[i], dt))[None, :]
+        D = 1e-3 * (s_abs + p + babs) + 1e-6 + p
+        lo, hi = _round_all(v - D, dt), _round_all(v + D, dt)
+        y = decode_bits(_bits(nodes[i]["y"]), dt)
+        bad = ~((decode_bits(lo, dt) <= y) & (y <= decode_bits(hi, dt)))
+        assert not bad.any(), f"node {i}: {bad.sum()} outputs outside the carried bound"
+        x_or = y_or.astype(np.uint16)
+        c = decode_bits(y_or, dt)
+        e = np.maximum(decode_bits(hi, dt) - c, c - decode_bits(lo, dt))
+    step.close()
+
+
+def _decoder_nodes(layers, batch, seed):
+    """Two decoder layers' linear layers with GPU-quantized weights: q, k, v
+    from the layer input; o from q; gate and up from o; down from gate; the
+    next layer's input is down's output."""
+    import w4a16_gemv_gb300 as nf4
+    code2 = u16_to_torch(synth.code2_linear(), torch.float16)
+    shapes = [(l.N, l.K) for l in synth.QWEN_1P5B_LAYERS]  # q k v o gate up down
+    inputs = [-1, -1, -1, 0, 3, 3, 4]                       # index within the layer
+    nodes = []
+    for layer in range(layers):
+        base = 7 * layer
+        for j, (N, K) in enumerate(shapes):
+            g = torch.Generator(device="cpu").manual_seed(seed + base + j)
+            w = (torch.randn(N * K, generator=g) * 0.02).to(dev())
+            wt = nf4.nf4_quantize(w, code2)
+            wt.shape = (N, K)
+            inp = inputs[j]
+            if inp == -1:
+                inp = -1 if layer == 0 else base - 1       # previous layer's down_proj
+            else:
+                inp = base + inp
+            bias = None
+            if j < 3:                                      # q, k, v carry a bias
+                bias = (torch.randn(N, generator=g) * 0.5).bfloat16().to(dev())
+            y = torch.empty((batch, N), dtype=torch.bfloat16, device=dev())
+            nodes.append(dict(weight=wt, y=y, bias=bias, input=inp))
+    return nodes
+
+
+@pytest.mark.parametrize("batch", [1, 3])
+def test_replays_equal_node_by_node_launches(batch):
+    import w4a16_gemv_gb300 as nf4
+    nodes = _decoder_nodes(2, batch, 300)
+    x = torch.empty((batch, 1536), dtype=torch.bfloat16, device=dev())
+    step = nf4.DecodeStep(nodes, x)
+    ref = [torch.empty_like(nd["y"]) for nd in nodes]
+    stream = torch.cuda.Stream()
+    for rep in range(3):
+        g = torch.Generator(device="cpu").manual_seed(400 + rep)
+        x.copy_(torch.randn((batch, 1536), generator=g).bfloat16())
+        for nd in nodes:
+            nd["y"].fill_(float("nan"))
+        with torch.cuda.stream(stream):
+            step.launch(stream)
+        stream.synchronize()
+        for i, nd in enumerate(nodes):
+            src = x if nd["input"] == -1 else ref[nd["input"]]
+            wt = nd["weight"]
+            N, K = wt.shape
+            nf4.nf4_gemv_ex(wt.packed, wt.absmax_q, wt.absmax2, wt.code2, wt.offset, N, K, src,
+                            bias=nd["bias"], y=ref[i], out_dtype=torch.bfloat16)
+        torch.cuda.synchronize()
+        for i, nd in enumerate(nodes):
+            assert torch.equal(nd["y"].view(torch.int16), ref[i].view(torch.int16)), (rep, i)
+    step.close()
+
+
+def test_many_replays_back_to_back_and_empty_nodes():
+    """Replays queued without synchronisation run in order (each replay's
+    input is written by a copy queued before it), and empty nodes are skipped."""
+    import w4a16_gemv_gb300 as nf4
+    N, K = 512, 1536
+    t = oracle.quantize(synth.weights(500, N * K), 64, 256, synth.code2_linear())
+    wt = _weight(t, N, K)
+    x = torch.empty((1, K), dtype=torch.bfloat16, device=dev())
+    y = torch.empty((1, N), dtype=torch.float32, device=dev())
+    empty = nf4.NF4Weight(wt.packed, wt.absmax_q, wt.absmax2, wt.code2, wt.offset, 0, (0, K))
+    y0 = torch.empty((1, 0), dtype=torch.bfloat16, device=dev())
+    step = nf4.DecodeStep([dict(weight=empty, y=y0), dict(weight=wt, y=y)], x)
+    xs = [synth.activations(510 + r, 1, K) for r in range(8)]
+    outs = []
+    s = torch.cuda.current_stream()
+    for r in range(8):
+        x.copy_(u16_to_torch(xs[r], torch.bfloat16).view(1, K), non_blocking=True)
+        step.launch(s)
+        outs.append(y.clone())
+    torch.cuda.synchronize()
+    for r in range(8):
+        y_ref, s_abs = oracle.gemv(t, N, K, xs[r])
+        err = np.abs(outs[r].cpu().numpy().astype(np.float64) - y_ref)
+        assert np.all(err <= 1e-3 * s_abs + 1e-6), r
+    step.close()

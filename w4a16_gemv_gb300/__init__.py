@@ -14,7 +14,7 @@ from dataclasses import dataclass
 
 import torch
 
-__all__ = ["NF4Error", "NF4Weight", "nf4_dequant", "nf4_gemv", "nf4_gemv_ex", "nf4_quantize",
+__all__ = ["NF4Error", "NF4Weight", "nf4_dequant", "nf4_gemv", "nf4_gemv_ex", "DecodeStep", "nf4_quantize",
            "nf4_quantize_workspace_size", "nf4_quantize_noalloc", "nf4_version", "nf4_status_string",
            "nf4_device_error_flags", "LIB_PATH"]
 
@@ -38,6 +38,22 @@ _lib.nf4_gemv.restype = ctypes.c_int
 _lib.nf4_gemv_ex.argtypes = [_P, _P, _P, _P, ctypes.c_float, _I64, _I64, _I32, _I32, _P, _I32, _P, _P,
                              ctypes.c_int, _P]
 _lib.nf4_gemv_ex.restype = ctypes.c_int
+
+
+class _GemvNode(ctypes.Structure):
+    """nf4_gemv_node of include/nf4.h."""
+    _fields_ = [("packed", _P), ("absmax_q", _P), ("absmax2", _P), ("code2", _P),
+                ("offset", ctypes.c_float), ("N", _I64), ("K", _I64), ("blocksize", _I32),
+                ("s2_blocksize", _I32), ("bias", _P), ("input", _I32), ("y", _P),
+                ("y_dtype", ctypes.c_int)]
+
+
+_lib.nf4_step_create.argtypes = [ctypes.POINTER(_GemvNode), _I32, _P, _I32, ctypes.POINTER(_P)]
+_lib.nf4_step_create.restype = ctypes.c_int
+_lib.nf4_step_launch.argtypes = [_P, _P]
+_lib.nf4_step_launch.restype = ctypes.c_int
+_lib.nf4_step_destroy.argtypes = [_P]
+_lib.nf4_step_destroy.restype = ctypes.c_int
 _lib.nf4_quantize_workspace_size.argtypes = [_I64, _I32, _I32]
 _lib.nf4_quantize_workspace_size.restype = ctypes.c_size_t
 _lib.nf4_quantize.argtypes = [_P, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
@@ -196,6 +212,58 @@ def nf4_gemv_ex(packed, absmax_q, absmax2, code2, offset: float, N: int, K: int,
                           _ptr(y, "y", out_dtype, batch * N), _Y_DTYPES[out_dtype], _stream(stream))
     _check(st, "nf4_gemv_ex")
     return y
+
+
+class DecodeStep:
+    """A fixed sequence of fused GEMV nodes recorded once into a CUDA graph
+    (nf4_step_create) and replayed with ``launch()`` (nf4_step_launch).
+
+    ``nodes`` is a list of dicts: ``weight`` (NF4Weight of shape (N, K)), ``y`` (CUDA tensor
+    [batch, N] of bf16, fp16 or fp32), optional ``bias`` ([N], y's dtype) and ``input`` (-1 for
+    the step input ``x``, else the index of an earlier node whose bf16 ``y`` is this node's x).
+    The tensors are referenced, not copied: replays read their current contents.
+    """
+
+    def __init__(self, nodes: list, x: torch.Tensor):
+        if x.dim() == 1:
+            x = x.view(1, -1)
+        batch = x.shape[0]
+        arr = (_GemvNode * len(nodes))()
+        self._keep = [x]
+        for i, nd in enumerate(nodes):
+            wt, y = nd["weight"], nd["y"]
+            N, K = wt.shape
+            inp = int(nd.get("input", -1))
+            if y.dtype not in _Y_DTYPES:
+                raise TypeError(f"node {i}: y must be bf16, fp16 or fp32")
+            if inp == -1 and x.shape[1] != K:
+                raise ValueError(f"node {i}: x has {x.shape[1]} columns, expected K={K}")
+            n = N * K
+            nbytes, nb, ng = _sizes(n, wt.blocksize, wt.s2_blocksize) if n > 0 else (0, 0, 0)
+            bias = nd.get("bias")
+            arr[i] = _GemvNode(_ptr(wt.packed, "packed", torch.uint8, nbytes),
+                               _ptr(wt.absmax_q, "absmax_q", torch.uint8, nb),
+                               _ptr(wt.absmax2, "absmax2", torch.float16, ng),
+                               _ptr(wt.code2, "code2", torch.float16, 256), float(wt.offset), N, K,
+                               wt.blocksize, wt.s2_blocksize, _ptr(bias, "bias", y.dtype, N), inp,
+                               _ptr(y, "y", y.dtype, batch * N), _Y_DTYPES[y.dtype])
+            self._keep += [wt, y, bias]
+        h = _P()
+        st = _lib.nf4_step_create(arr, len(nodes), _ptr(x, "x", torch.bfloat16, x.numel()),
+                                  int(batch), ctypes.byref(h))
+        _check(st, "nf4_step_create")
+        self._h = h
+
+    def launch(self, stream=None) -> None:
+        _check(_lib.nf4_step_launch(self._h, _stream(stream)), "nf4_step_launch")
+
+    def close(self) -> None:
+        if getattr(self, "_h", None) is not None and self._h.value:
+            _lib.nf4_step_destroy(self._h)
+        self._h = None
+
+    def __del__(self):
+        self.close()
 
 
 def nf4_quantize_workspace_size(n: int, blocksize: int = 64, s2_blocksize: int = 256) -> int:

@@ -104,11 +104,15 @@ nf4_status nf4_dequant(const uint8_t* packed, const uint8_t* absmax_q, const uin
   return cuda_status(nf4::launch_dequant(t, n, out, out_dtype, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-nf4_status nf4_gemv_ex(const uint8_t* packed, const uint8_t* absmax_q, const uint16_t* absmax2,
-                       const uint16_t* code2, float offset, int64_t N, int64_t K,
-                       int32_t blocksize, int32_t s2_blocksize, const uint16_t* x,
-                       int32_t batch, const void* bias, void* y, nf4_dtype y_dtype,
-                       nf4_stream_t stream) {
+}  // extern "C"
+
+namespace nf4 {
+
+nf4_status check_gemv_args(const uint8_t* packed, const uint8_t* absmax_q,
+                           const uint16_t* absmax2, const uint16_t* code2, float offset, int64_t N,
+                           int64_t K, int32_t blocksize, int32_t s2_blocksize, const uint16_t* x,
+                           int32_t batch, const void* bias, void* y, nf4_dtype y_dtype,
+                           QuantTensor* t, YOut* out) {
   if (N < 0 || K < 0 || (K & 1) != 0) return NF4_ERR_INVALID_SIZE;
   if (K > 0 && N > kMaxElems / K) return NF4_ERR_INVALID_SIZE;
   if (N > kMaxElems) return NF4_ERR_INVALID_SIZE;
@@ -128,8 +132,28 @@ nf4_status nf4_gemv_ex(const uint8_t* packed, const uint8_t* absmax_q, const uin
     if (!x) return NF4_ERR_NULL;
     if (!aligned(x, 2)) return NF4_ERR_MISALIGNED;
   }
-  const nf4::QuantTensor t{packed, absmax_q, absmax2, code2, offset, lbs, ls2};
-  const nf4::YOut out{y, bias, int(y_dtype)};
+  *t = QuantTensor{packed, absmax_q, absmax2, code2, offset, lbs, ls2};
+  *out = YOut{y, bias, int(y_dtype)};
+  return NF4_OK;
+}
+
+nf4_status status_of(cudaError_t e) { return cuda_status(e); }
+
+}  // namespace nf4
+
+extern "C" {
+
+nf4_status nf4_gemv_ex(const uint8_t* packed, const uint8_t* absmax_q, const uint16_t* absmax2,
+                       const uint16_t* code2, float offset, int64_t N, int64_t K,
+                       int32_t blocksize, int32_t s2_blocksize, const uint16_t* x,
+                       int32_t batch, const void* bias, void* y, nf4_dtype y_dtype,
+                       nf4_stream_t stream) {
+  nf4::QuantTensor t;
+  nf4::YOut out;
+  const nf4_status st = nf4::check_gemv_args(packed, absmax_q, absmax2, code2, offset, N, K,
+                                             blocksize, s2_blocksize, x, batch, bias, y, y_dtype,
+                                             &t, &out);
+  if (st != NF4_OK || N == 0) return st;
   return cuda_status(
       nf4::launch_gemv(t, N, K, x, batch, out, reinterpret_cast<cudaStream_t>(stream)));
 }
