@@ -166,3 +166,43 @@ def test_many_replays_back_to_back_and_empty_nodes():
         err = np.abs(outs[r].cpu().numpy().astype(np.float64) - y_ref)
         assert np.all(err <= 1e-3 * s_abs + 1e-6), r
     step.close()
+
+
+@pytest.mark.parametrize("batch", [1, 2, 4, 8])
+@pytest.mark.parametrize("Ns", [(1536, 256, 256), (37, 1, 300, 1000, 5), (5, 7), (8960, 8960)])
+def test_grouped_nodes_against_the_oracle(Ns, batch):
+    """Consecutive nodes reading the same x run as one grouped launch (up to
+    four weights; CTAs spread over them by rows); each output is checked
+    against the oracle, with mixed output types and biases."""
+    import w4a16_gemv_gb300 as nf4
+    K = 1536
+    x_bits = synth.activations(600 + batch, batch, K)
+    x = u16_to_torch(x_bits, torch.bfloat16).view(batch, K)
+    kinds = [(BF16, True), (FP16, False), (F32, True), (BF16, False), (FP16, True)]
+    ts, nodes, biases = [], [], []
+    for j, N in enumerate(Ns):
+        dt, has_bias = kinds[j % len(kinds)]
+        t = oracle.quantize(synth.weights(610 + j + N, N * K), 64, 256, synth.code2_linear())
+        ts.append(t)
+        name = {BF16: "bf16", FP16: "fp16", F32: "f32"}[dt]
+        b = synth.bias(620 + j, N, name) if has_bias else None
+        biases.append(b)
+        bt = None
+        if b is not None:
+            bt = torch.from_numpy(b.view(np.int32 if dt == F32 else np.int16)).to(dev()).view(_TDT[dt])
+        y = torch.full((batch, N), float("nan"), dtype=_TDT[dt], device=dev())
+        nodes.append(dict(weight=_weight(t, N, K), y=y, bias=bt, input=-1))
+    step = nf4.DecodeStep(nodes, x)
+    step.launch()
+    torch.cuda.synchronize()
+    for j, N in enumerate(Ns):
+        dt = kinds[j % len(kinds)][0]
+        y_ref, s_abs = oracle.gemv(ts[j], N, K, x_bits)
+        v, _ = oracle.gemv_output(y_ref, dt, biases[j])
+        babs = 0.0 if biases[j] is None else np.abs(decode_bits(biases[j], dt))[None, :]
+        tol = 1e-3 * (s_abs + babs) + 1e-6
+        lo, hi = _round_all(v - tol, dt), _round_all(v + tol, dt)
+        y = decode_bits(_bits(nodes[j]["y"]), dt)
+        bad = ~((decode_bits(lo, dt) <= y) & (y <= decode_bits(hi, dt)))
+        assert not bad.any(), f"node {j} (N={N}): {bad.sum()} outputs outside tolerance"
+    step.close()

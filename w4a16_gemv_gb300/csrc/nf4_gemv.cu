@@ -357,8 +357,9 @@ cudaError_t dispatch_batch(const QuantTensor& t, int64_t N, int64_t K, const uin
   }
   {
     bool done = false;
-    const cudaError_t ek = (B == 1) ? try_gemv_b1(t, N, K, x, y, sms, stream, &done)
-                                    : try_gemv_bn(t, N, K, x, B, y, sms, stream, &done);
+    const SubTensor one{t, y, N, 0, 0};
+    const cudaError_t ek = (B == 1) ? try_gemv_b1(&one, 1, K, x, sms, stream, &done)
+                                    : try_gemv_bn(&one, 1, K, x, B, sms, stream, &done);
     if (done || ek != cudaSuccess) return ek;
   }
   const FastConfig f = choose_config(t, N, K, B, x, sms);
@@ -416,6 +417,19 @@ cudaError_t launch_gemv(const QuantTensor& t, int64_t N, int64_t K, const uint16
     case 8: return dispatch_batch<8>(t, N, K, x, y, stream);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_gemv_group(const QuantTensor* ts, const int64_t* Ns, const YOut* outs, int n,
+                              int64_t K, const uint16_t* x, int batch, cudaStream_t stream,
+                              bool* done) {
+  *done = false;
+  if (n < 1 || n > kMaxSub || K <= 0 || batch < 1 || batch > 8) return cudaSuccess;
+  const int sms = device_sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  SubTensor subs[kMaxSub];
+  for (int j = 0; j < n; ++j) subs[j] = SubTensor{ts[j], outs[j], Ns[j], 0, 0};
+  return batch == 1 ? try_gemv_b1(subs, n, K, x, sms, stream, done)
+                    : try_gemv_bn(subs, n, K, x, batch, sms, stream, done);
 }
 
 }  // namespace nf4

@@ -50,17 +50,28 @@ namespace {
 #endif
 
 constexpr int kMaxGroups = 15;         // named barriers 1..15
+
+// The weight CTA `cta` serves, selected with compile-time indices only (no
+// dynamic indexing of the parameter block).
+template <int NSUB>
+__device__ __forceinline__ SubTensor pick_sub(const SubTensor (&s)[kMaxSub], int nsub, int cta) {
+  SubTensor v = s[0];
+#pragma unroll
+  for (int i = 1; i < NSUB; ++i)
+    if (i < nsub && cta >= s[i].cta0) v = s[i];
+  return v;
+}
 constexpr uint32_t kTabBytes = 65536;  // 256 rows of 256 B
 constexpr int kMaxSmemPerCta = 227 * 1024;
 
-// Everything a launch needs, in one argument block.
+// Everything a launch needs, in one argument block. A launch serves one to
+// kMaxSub weights that share x (a grouped launch): CTAs [cta0, cta0 + ctas)
+// serve weight j, CTA cta0 + b owning its rows [b*N/ctas, (b+1)*N/ctas).
 struct B1Args {
-  QuantTensor t;
+  SubTensor sub[kMaxSub];
+  int nsub;
   const uint16_t* x;
-  YOut out;
-  int64_t N;
   int32_t K;
-  int grid;  // CTAs; CTA b owns rows [b*N/grid, (b+1)*N/grid)
   int W;     // warps per row group (32 * W >= chunks per row)
   int G;     // row groups
   int spr;   // quantization blocks per row
@@ -70,8 +81,75 @@ struct B1Args {
 
 struct B1Plan {
   B1Args a;
+  int grid;
   uint32_t smem_bytes;
 };
+
+bool any_bias(const SubTensor* subs, int nsub) {
+  for (int j = 0; j < nsub; ++j)
+    if (subs[j].out.bias) return true;
+  return false;
+}
+
+// Spreads one wave of CTAs (at most `sms`) over the weights of a launch in
+// proportion to their rows, at least one CTA per weight and at most one per
+// row, and fills cta0 / ctas of out[]. Returns the largest number of rows a
+// CTA owns, or -1 when the weights cannot share a launch (an empty weight,
+// or block sizes that differ).
+int assign_ctas(const SubTensor* subs, int nsub, int sms, SubTensor* out, int* grid_out) {
+  if (nsub < 1 || nsub > kMaxSub || sms < nsub) return -1;
+  int64_t total = 0;
+  for (int j = 0; j < nsub; ++j) {
+    if (subs[j].N <= 0 || subs[j].t.lbs != subs[0].t.lbs || subs[j].t.ls2 != subs[0].t.ls2)
+      return -1;
+    total += subs[j].N;
+  }
+  const int grid = int(total < sms ? total : sms);
+  int ctas[kMaxSub];
+  int used = 0;
+  for (int j = 0; j < nsub; ++j) {
+    int64_t c = int64_t(grid) * subs[j].N / total;
+    if (c < 1) c = 1;
+    if (c > subs[j].N) c = subs[j].N;
+    ctas[j] = int(c);
+    used += ctas[j];
+  }
+  // rows per CTA of weight j with c CTAs, rounded up
+  auto load = [&](int j, int c) { return (subs[j].N + c - 1) / c; };
+  while (used < grid) {  // give the spare CTAs to the most loaded weights
+    int best = -1;
+    for (int j = 0; j < nsub; ++j)
+      if (ctas[j] < subs[j].N && (best < 0 || load(j, ctas[j]) > load(best, ctas[best]))) best = j;
+    if (best < 0) break;
+    ++ctas[best];
+    ++used;
+  }
+  while (used > grid) {  // take back from the least loaded
+    int best = -1;
+    for (int j = 0; j < nsub; ++j)
+      if (ctas[j] > 1 && (best < 0 || load(j, ctas[j] - 1) < load(best, ctas[best] - 1))) best = j;
+    if (best < 0) return -1;
+    --ctas[best];
+    --used;
+  }
+  int64_t max_rows = 0;
+  int c0 = 0;
+  for (int j = 0; j < kMaxSub; ++j) {
+    if (j < nsub) {
+      out[j] = subs[j];
+      out[j].cta0 = c0;
+      out[j].ctas = ctas[j];
+      c0 += ctas[j];
+      const int64_t r = load(j, ctas[j]);
+      if (r > max_rows) max_rows = r;
+    } else {
+      out[j] = out[0];
+      out[j].cta0 = used;  // never selected: past the last CTA
+    }
+  }
+  *grid_out = used;
+  return max_rows > (int64_t(1) << 30) ? -1 : int(max_rows);
+}
 
 __device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
   uint32_t v;
@@ -310,7 +388,7 @@ __device__ __forceinline__ void consume(const B1Args& p, const uint8_t* lane_src
   }
 }
 
-template <int CB, int RPG, int kThreads>
+template <int CB, int RPG, int kThreads, int NSUB>
 __global__ void __launch_bounds__(kThreads, 1) gemv_b1_kernel(const B1Args p) {
   constexpr int CE = 2 * CB;  // elements per column chunk
   extern __shared__ __align__(128) unsigned char smem[];
@@ -338,9 +416,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_b1_kernel(const B1Args p) {
   }
   pdl_allow_dependents();
 
-  const QuantTensor& t = p.t;
+  const SubTensor sb = pick_sub<NSUB>(p.sub, p.nsub, int(blockIdx.x));
+  const QuantTensor& t = sb.t;
   const uint16_t* __restrict__ x = p.x;
-  const int64_t N = p.N;
+  const int64_t N = sb.N;
   const int64_t K = p.K;
   float* sC2 = reinterpret_cast<float*>(smem + p.off_c2);
   float* sA2 = reinterpret_cast<float*>(smem + p.off_a2);
@@ -351,8 +430,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_b1_kernel(const B1Args p) {
   uint32_t* sBias = reinterpret_cast<uint32_t*>(smem + p.off_bias);
 
   const int64_t row_bytes = K >> 1;
-  const int64_t row_begin = (int64_t(blockIdx.x) * N) / p.grid;
-  const int64_t row_end = (int64_t(blockIdx.x + 1) * N) / p.grid;
+  const int64_t bid = int64_t(blockIdx.x) - sb.cta0;
+  const int64_t row_begin = (bid * N) / sb.ctas;
+  const int64_t row_end = ((bid + 1) * N) / sb.ctas;
   const int nrows = int(row_end - row_begin);
   const int64_t b0 = (row_begin * K) >> t.lbs;  // first quantization block of the CTA
   const int nq = nrows * p.spr;
@@ -414,8 +494,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_b1_kernel(const B1Args p) {
   else if (tid >= 32 && tid - 32 < nq - q_mid_end) qi = q_mid_end + (tid - 32);
   const uint8_t qb = qi >= 0 ? ldg_u8_ordered(t.absmax_q + b0 + qi) : uint8_t(0);
   // bias of the CTA's rows, kept (as stored) in shared memory for the end
-  const bool has_bias = p.out.bias != nullptr;
-  const uint32_t bias_v = (has_bias && tid < nrows) ? bias_bits_ordered(p.out, row_begin + tid) : 0u;
+  const bool has_bias = sb.out.bias != nullptr;
+  const uint32_t bias_v = (has_bias && tid < nrows) ? bias_bits_ordered(sb.out, row_begin + tid) : 0u;
   // Shared copies of the small inputs (further batches for long ranges).
   if (tid < 256) sC2[tid] = half_bits_to_float(c2v);
 #pragma unroll
@@ -427,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_b1_kernel(const B1Args p) {
   if (qi >= 0) sQ[q_lead + qi] = qb;
   if (has_bias) {
     if (tid < nrows) sBias[tid] = bias_v;
-    for (int i = tid + kThreads; i < nrows; i += kThreads) sBias[i] = y_bias_bits(p.out, row_begin + i);
+    for (int i = tid + kThreads; i < nrows; i += kThreads) sBias[i] = y_bias_bits(sb.out, row_begin + i);
   }
   for (int base = 4 * kThreads; base < ng; base += 4 * kThreads) {  // small group sizes only
 #pragma unroll
@@ -556,7 +636,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_b1_kernel(const B1Args p) {
   for (int r = rg0 + gt; r < rg1; r += p.W * 32) {
     float v = 0.0f;
     for (int w = 0; w < p.W; ++w) v += sPart[r * p.W + w];
-    y_store(p.out, row_begin + r, v, has_bias ? sBias[r] : 0u);
+    y_store(sb.out, row_begin + r, v, has_bias ? sBias[r] : 0u);
   }
 }
 
@@ -577,28 +657,27 @@ int reserved_smem_per_block() {
 // sums] below the pair table (+ binary16 x) at shared window address 64 KB.
 // The dynamic window starts after the per-block reserved shared memory (the
 // kernel has no static shared variables).
-bool plan_b1(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x, const YOut& out,
-             int cb, int threads, int sms, B1Plan* plan) {
+bool plan_b1(const SubTensor* subs, int nsub, int64_t K, const uint16_t* x, int cb, int threads,
+             int sms, B1Plan* plan) {
   const int kWarps = threads / 32;
   B1Args* p = &plan->a;
+  const QuantTensor& t = subs[0].t;
   const int64_t bs = int64_t(1) << t.lbs;
   const int ce = 2 * cb;
-  if (N <= 0 || K % 32 != 0 || K % bs != 0 || bs < ce || K > 16384) return false;
+  if (K % 32 != 0 || K % bs != 0 || bs < ce || K > 16384) return false;
   const int64_t cpr = K / ce;
   const int W = int((cpr + 31) / 32);
   if (W > kWarps) return false;
   int G = kWarps / W;
   if (G > kMaxGroups) G = kMaxGroups;
-  p->t = t;
+  const int max_rows = assign_ctas(subs, nsub, sms, p->sub, &plan->grid);
+  if (max_rows <= 0) return false;
+  p->nsub = nsub;
   p->x = x;
-  p->out = out;
-  p->N = N;
   p->K = int32_t(K);
   p->W = W;
   p->cpr = int(cpr);
   p->spr = int(K / bs);
-  p->grid = int(N < sms ? N : sms);
-  const int max_rows = int((N + p->grid - 1) / p->grid);
   if (G > max_rows) G = max_rows;
   p->G = G;
   const int64_t max_nq = int64_t(max_rows) * p->spr;
@@ -620,7 +699,7 @@ bool plan_b1(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x, cons
   p->off_part = off;
   off += align_up_u32(uint32_t(max_rows * W * 4), 128);
   p->off_bias = off;
-  if (out.bias) off += align_up_u32(uint32_t(max_rows * 4), 128);
+  if (any_bias(subs, nsub)) off += align_up_u32(uint32_t(max_rows * 4), 128);
   const uint32_t tab = 65536u - uint32_t(res);
   if (off > tab) return false;
   p->off_tab = tab;
@@ -628,9 +707,9 @@ bool plan_b1(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x, cons
   return plan->smem_bytes <= uint32_t(kMaxSmemPerCta);
 }
 
-template <int CB, int NT>
+template <int CB, int NT, int NSUB>
 cudaError_t launch_b1(const B1Plan& plan, cudaStream_t stream) {
-  auto kern = gemv_b1_kernel<CB, NF4_B1_RPG, NT>;
+  auto kern = gemv_b1_kernel<CB, NF4_B1_RPG, NT, NSUB>;
   static int attr_set[64] = {0};
   int dev = 0;
   const cudaError_t ed = cudaGetDevice(&dev);
@@ -641,7 +720,7 @@ cudaError_t launch_b1(const B1Plan& plan, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = 1;
   }
-  return launch_k(kern, dim3(unsigned(plan.a.grid)), dim3(unsigned(NT)), plan.smem_bytes, stream,
+  return launch_k(kern, dim3(unsigned(plan.grid)), dim3(unsigned(NT)), plan.smem_bytes, stream,
                   plan.a);
 }
 
@@ -741,15 +820,13 @@ __device__ __forceinline__ void consume_n(const uint8_t* lane_src, uint32_t row_
   }
 }
 
-// Arguments of the batched kernel.
+// Arguments of the batched kernel (grouped launches as for batch 1).
 struct BNArgs {
-  QuantTensor t;
+  SubTensor sub[kMaxSub];
+  int nsub;
   const uint16_t* x;
-  YOut out;
-  int64_t N;
   int32_t K;
   int batch;   // real vectors (<= BP)
-  int grid;    // CTAs; CTA b owns rows [b*N/grid, (b+1)*N/grid)
   int W;       // warps per row group (per slice)
   int G;       // row groups
   int spr;     // quantization blocks per row
@@ -758,7 +835,7 @@ struct BNArgs {
   uint32_t off_c2, off_a2, off_q, off_scale, off_part, off_bias, off_tab;
 };
 
-template <int BP, int CB, int RPG>
+template <int BP, int CB, int RPG, int NSUB>
 __global__ void __launch_bounds__(512, 1) gemv_bn_kernel(const BNArgs p) {
   constexpr int kThreads = 512;
   constexpr int CE = 2 * CB;
@@ -783,8 +860,9 @@ __global__ void __launch_bounds__(512, 1) gemv_bn_kernel(const BNArgs p) {
   }
   pdl_allow_dependents();
 
-  const QuantTensor& t = p.t;
-  const int64_t N = p.N;
+  const SubTensor sb = pick_sub<NSUB>(p.sub, p.nsub, int(blockIdx.x));
+  const QuantTensor& t = sb.t;
+  const int64_t N = sb.N;
   const int64_t K = p.K;
   float* sC2 = reinterpret_cast<float*>(smem + p.off_c2);
   float* sA2 = reinterpret_cast<float*>(smem + p.off_a2);
@@ -794,8 +872,9 @@ __global__ void __launch_bounds__(512, 1) gemv_bn_kernel(const BNArgs p) {
   uint32_t* sBias = reinterpret_cast<uint32_t*>(smem + p.off_bias);
 
   const int64_t row_bytes = K >> 1;
-  const int64_t row_begin = (int64_t(blockIdx.x) * N) / p.grid;
-  const int64_t row_end = (int64_t(blockIdx.x + 1) * N) / p.grid;
+  const int64_t bid = int64_t(blockIdx.x) - sb.cta0;
+  const int64_t row_begin = (bid * N) / sb.ctas;
+  const int64_t row_end = ((bid + 1) * N) / sb.ctas;
   const int nrows = int(row_end - row_begin);
   const int64_t b0 = (row_begin * K) >> t.lbs;
   const int nq = nrows * p.spr;
@@ -839,8 +918,8 @@ __global__ void __launch_bounds__(512, 1) gemv_bn_kernel(const BNArgs p) {
   else if (tid >= 32 && tid - 32 < nq - q_mid_end) qi = q_mid_end + (tid - 32);
   const uint8_t qb = qi >= 0 ? ldg_u8_ordered(t.absmax_q + b0 + qi) : uint8_t(0);
   // bias of the CTA's rows, kept (as stored) in shared memory for the end
-  const bool has_bias = p.out.bias != nullptr;
-  const uint32_t bias_v = (has_bias && tid < nrows) ? bias_bits_ordered(p.out, row_begin + tid) : 0u;
+  const bool has_bias = sb.out.bias != nullptr;
+  const uint32_t bias_v = (has_bias && tid < nrows) ? bias_bits_ordered(sb.out, row_begin + tid) : 0u;
   if (tid < 256) sC2[tid] = half_bits_to_float(c2v);
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
@@ -851,7 +930,7 @@ __global__ void __launch_bounds__(512, 1) gemv_bn_kernel(const BNArgs p) {
   if (qi >= 0) sQ[q_lead + qi] = qb;
   if (has_bias) {
     if (tid < nrows) sBias[tid] = bias_v;
-    for (int i = tid + kThreads; i < nrows; i += kThreads) sBias[i] = y_bias_bits(p.out, row_begin + i);
+    for (int i = tid + kThreads; i < nrows; i += kThreads) sBias[i] = y_bias_bits(sb.out, row_begin + i);
   }
   for (int base = 4 * kThreads; base < ng; base += 4 * kThreads) {
 #pragma unroll
@@ -917,16 +996,17 @@ __global__ void __launch_bounds__(512, 1) gemv_bn_kernel(const BNArgs p) {
     if (b >= p.batch) continue;
     float v = 0.0f;
     for (int w = 0; w < p.W; ++w) v += sPart[(r * BP + b) * p.W + w];
-    y_store(p.out, int64_t(b) * N + row_begin + r, v, has_bias ? sBias[r] : 0u);
+    y_store(sb.out, int64_t(b) * N + row_begin + r, v, has_bias ? sBias[r] : 0u);
   }
 }
 
 // Plan for BP vectors and CB-byte chunks (512 threads, one CTA per SM).
-bool plan_bn(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x, int batch,
-             const YOut& out, int bp, int cb, int sms, BNArgs* p, uint32_t* smem_bytes) {
+bool plan_bn(const SubTensor* subs, int nsub, int64_t K, const uint16_t* x, int batch, int bp,
+             int cb, int sms, BNArgs* p, int* grid, uint32_t* smem_bytes) {
+  const QuantTensor& t = subs[0].t;
   const int64_t bs = int64_t(1) << t.lbs;
   const int ce = 2 * cb;
-  if (N <= 0 || K % 32 != 0 || K % bs != 0 || bs < ce) return false;
+  if (K % 32 != 0 || K % bs != 0 || bs < ce) return false;
   const int64_t cpr = K / ce;
   int W = int((cpr + 31) / 32);
   int slices = 1;
@@ -936,18 +1016,16 @@ bool plan_bn(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x, int 
   }
   int G = 16 / W;
   if (G > kMaxGroups) G = kMaxGroups;
-  p->t = t;
+  const int max_rows = assign_ctas(subs, nsub, sms, p->sub, grid);
+  if (max_rows <= 0) return false;
+  p->nsub = nsub;
   p->x = x;
-  p->out = out;
-  p->N = N;
   p->K = int32_t(K);
   p->batch = batch;
   p->W = W;
   p->cpr = int(cpr);
   p->slices = slices;
   p->spr = int(K / bs);
-  p->grid = int(N < sms ? N : sms);
-  const int max_rows = int((N + p->grid - 1) / p->grid);
   if (G > max_rows) G = max_rows;
   if (slices > 1) G = 1;
   p->G = G;
@@ -968,7 +1046,7 @@ bool plan_bn(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x, int 
   p->off_part = off;
   off += align_up_u32(uint32_t(max_rows * bp * W * 4), 128);
   p->off_bias = off;
-  if (out.bias) off += align_up_u32(uint32_t(max_rows * 4), 128);
+  if (any_bias(subs, nsub)) off += align_up_u32(uint32_t(max_rows * 4), 128);
   const uint32_t tab = 65536u - uint32_t(res);
   if (off > tab) return false;
   p->off_tab = tab;
@@ -976,10 +1054,8 @@ bool plan_bn(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x, int 
   return *smem_bytes <= uint32_t(kMaxSmemPerCta);
 }
 
-template <int BP, int CB>
-cudaError_t launch_bn(const BNArgs& a, uint32_t smem_bytes, cudaStream_t stream) {
-  auto kern = gemv_bn_kernel<BP, CB, 2>;
-  static int attr_set[64] = {0};
+template <typename Kern>
+cudaError_t set_smem_limit_once(Kern kern, int* attr_set) {
   int dev = 0;
   const cudaError_t ed = cudaGetDevice(&dev);
   if (ed != cudaSuccess) return ed;
@@ -989,55 +1065,74 @@ cudaError_t launch_bn(const BNArgs& a, uint32_t smem_bytes, cudaStream_t stream)
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = 1;
   }
-  return launch_k(kern, dim3(unsigned(a.grid)), dim3(512u), smem_bytes, stream, a);
+  return cudaSuccess;
 }
+
+template <int BP, int CB, int NSUB>
+cudaError_t launch_bn(const BNArgs& a, int grid, uint32_t smem_bytes, cudaStream_t stream) {
+  auto kern = gemv_bn_kernel<BP, CB, 2, NSUB>;
+  static int attr_set[64] = {0};
+  const cudaError_t e = set_smem_limit_once(kern, attr_set);
+  if (e != cudaSuccess) return e;
+  return launch_k(kern, dim3(unsigned(grid)), dim3(512u), smem_bytes, stream, a);
+}
+
+template <int BP, int CB>
+cudaError_t launch_bn_n(const BNArgs& a, int grid, uint32_t smem_bytes, cudaStream_t stream) {
+  return a.nsub == 1 ? launch_bn<BP, CB, 1>(a, grid, smem_bytes, stream)
+                     : launch_bn<BP, CB, kMaxSub>(a, grid, smem_bytes, stream);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
 
-cudaError_t try_gemv_b1(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x,
-                        const YOut& y, int sms, cudaStream_t stream, bool* done) {
+cudaError_t try_gemv_b1(const SubTensor* subs, int nsub, int64_t K, const uint16_t* x, int sms,
+                        cudaStream_t stream, bool* done) {
   *done = false;
-  if ((reinterpret_cast<uintptr_t>(t.packed) & 15u) != 0 || (reinterpret_cast<uintptr_t>(x) & 15u) != 0)
-    return cudaSuccess;
-  if (K % 32 != 0) return cudaSuccess;
+  if (!aligned16(x) || K % 32 != 0) return cudaSuccess;
+  for (int j = 0; j < nsub; ++j)
+    if (!aligned16(subs[j].t.packed)) return cudaSuccess;
   // chunk width: 16 bytes unless that leaves more than 10% of the lanes idle
   // (measured: more, narrower lanes only add per-row overhead)
   const int64_t cpr16 = K / 32;
   const int cb = (double(cpr16) / double((cpr16 + 31) / 32 * 32) >= 0.9) ? 16 : 8;
   B1Plan p;
-  if (cb == 16 && plan_b1(t, N, K, x, y, 16, 512, sms, &p)) {
+  const bool one = nsub == 1;
+  if (cb == 16 && plan_b1(subs, nsub, K, x, 16, 512, sms, &p)) {
     *done = true;
-    return launch_b1<16, 512>(p, stream);
+    return one ? launch_b1<16, 512, 1>(p, stream) : launch_b1<16, 512, kMaxSub>(p, stream);
   }
-  if (plan_b1(t, N, K, x, y, 8, 512, sms, &p)) {
+  if (plan_b1(subs, nsub, K, x, 8, 512, sms, &p)) {
     *done = true;
-    return launch_b1<8, 512>(p, stream);
+    return one ? launch_b1<8, 512, 1>(p, stream) : launch_b1<8, 512, kMaxSub>(p, stream);
   }
   return cudaSuccess;
 }
 
-cudaError_t try_gemv_bn(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x, int batch,
-                        const YOut& y, int sms, cudaStream_t stream, bool* done) {
+cudaError_t try_gemv_bn(const SubTensor* subs, int nsub, int64_t K, const uint16_t* x, int batch,
+                        int sms, cudaStream_t stream, bool* done) {
   *done = false;
-  if (batch < 2 || batch > 8) return cudaSuccess;
-  if ((reinterpret_cast<uintptr_t>(t.packed) & 15u) != 0 || (reinterpret_cast<uintptr_t>(x) & 15u) != 0)
-    return cudaSuccess;
+  if (batch < 2 || batch > 8 || !aligned16(x)) return cudaSuccess;
+  for (int j = 0; j < nsub; ++j)
+    if (!aligned16(subs[j].t.packed)) return cudaSuccess;
   // x chunk of all BP vectors in registers: BP * 2 CB binary32 values = 64
   BNArgs a;
+  int grid = 0;
   uint32_t smem = 0;
   if (batch == 2) {
-    if (!plan_bn(t, N, K, x, batch, y, 2, 16, sms, &a, &smem)) return cudaSuccess;
+    if (!plan_bn(subs, nsub, K, x, batch, 2, 16, sms, &a, &grid, &smem)) return cudaSuccess;
     *done = true;
-    return launch_bn<2, 16>(a, smem, stream);
+    return launch_bn_n<2, 16>(a, grid, smem, stream);
   }
   if (batch <= 4) {
-    if (!plan_bn(t, N, K, x, batch, y, 4, 8, sms, &a, &smem)) return cudaSuccess;
+    if (!plan_bn(subs, nsub, K, x, batch, 4, 8, sms, &a, &grid, &smem)) return cudaSuccess;
     *done = true;
-    return launch_bn<4, 8>(a, smem, stream);
+    return launch_bn_n<4, 8>(a, grid, smem, stream);
   }
-  if (!plan_bn(t, N, K, x, batch, y, 8, 4, sms, &a, &smem)) return cudaSuccess;
+  if (!plan_bn(subs, nsub, K, x, batch, 8, 4, sms, &a, &grid, &smem)) return cudaSuccess;
   *done = true;
-  return launch_bn<8, 4>(a, smem, stream);
+  return launch_bn_n<8, 4>(a, grid, smem, stream);
 }
 
 cudaError_t read_and_clear_b1_flags(unsigned int* flags) {

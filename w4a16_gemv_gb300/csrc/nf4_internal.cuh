@@ -207,13 +207,30 @@ constexpr long long kWaitLimitCycles = 2000000000ll;
 cudaError_t read_and_clear_device_flags(unsigned int* flags);
 cudaError_t read_and_clear_b1_flags(unsigned int* flags);
 
-// Batch-1 GEMV (k-stationary, bulk-copy pipelined). Sets *done when it
-// handled the call; otherwise the caller uses the general kernels.
-cudaError_t try_gemv_b1(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x,
-                        const YOut& out, int sms, cudaStream_t stream, bool* done);
-// Batch 2..8 GEMV (k-stationary, binary32 x in registers, column slices).
-cudaError_t try_gemv_bn(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x, int batch,
-                        const YOut& out, int sms, cudaStream_t stream, bool* done);
+// One weight of a GEMV launch that may serve several weights sharing x.
+struct SubTensor {
+  QuantTensor t;
+  YOut out;
+  int64_t N;
+  int cta0;  // first CTA serving this weight (set by the planner)
+  int ctas;  // CTAs serving it (set by the planner)
+};
+constexpr int kMaxSub = 4;
+
+// Batch-1 GEMV (k-stationary, direct weight loads) of 1..kMaxSub weights
+// sharing x and K, in one launch. Sets *done when it handled the call;
+// otherwise the caller uses the general kernels (one launch per weight).
+cudaError_t try_gemv_b1(const SubTensor* subs, int nsub, int64_t K, const uint16_t* x, int sms,
+                        cudaStream_t stream, bool* done);
+// Batch 2..8 GEMV (k-stationary, binary32 x in registers, column slices),
+// grouped as for batch 1.
+cudaError_t try_gemv_bn(const SubTensor* subs, int nsub, int64_t K, const uint16_t* x, int batch,
+                        int sms, cudaStream_t stream, bool* done);
+// Several weights sharing x and K in one launch of the streaming kernels;
+// *done is false (nothing launched) when they cannot share one.
+cudaError_t launch_gemv_group(const QuantTensor* ts, const int64_t* Ns, const YOut* outs, int n,
+                              int64_t K, const uint16_t* x, int batch, cudaStream_t stream,
+                              bool* done);
 
 }  // namespace nf4
 

@@ -86,10 +86,31 @@ nf4_status nf4_step_create(const nf4_gemv_node* nodes, int32_t n_nodes, const ui
     e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed);
     if (e == cudaSuccess) {
       cudaError_t le = cudaSuccess;
-      for (int32_t i = 0; i < n_nodes && le == cudaSuccess; ++i) {
-        if (nodes[i].N == 0) continue;
-        le = nf4::launch_gemv(ts[size_t(i)], nodes[i].N, nodes[i].K, xs[size_t(i)], batch,
-                              outs[size_t(i)], cs);
+      for (int32_t i = 0; i < n_nodes && le == cudaSuccess;) {
+        if (nodes[i].N == 0) {
+          ++i;
+          continue;
+        }
+        // Consecutive nodes reading the same input (e.g. q/k/v, gate/up)
+        // share one launch when the streaming kernels can take them.
+        int32_t n = 1;
+        while (n < nf4::kMaxSub && i + n < n_nodes && nodes[i + n].N > 0 &&
+               nodes[i + n].input == nodes[i].input && nodes[i + n].K == nodes[i].K &&
+               nodes[i + n].blocksize == nodes[i].blocksize &&
+               nodes[i + n].s2_blocksize == nodes[i].s2_blocksize)
+          ++n;
+        bool done = false;
+        if (n > 1 && nodes[i].K > 0) {
+          int64_t Ns[nf4::kMaxSub];
+          for (int32_t j = 0; j < n; ++j) Ns[j] = nodes[i + j].N;
+          le = nf4::launch_gemv_group(&ts[size_t(i)], Ns, &outs[size_t(i)], int(n), nodes[i].K,
+                                      xs[size_t(i)], batch, cs, &done);
+        }
+        if (!done) n = 1;
+        if (le == cudaSuccess && !done)
+          le = nf4::launch_gemv(ts[size_t(i)], nodes[i].N, nodes[i].K, xs[size_t(i)], batch,
+                                outs[size_t(i)], cs);
+        i += n;
       }
       const cudaError_t ee = cudaStreamEndCapture(cs, &s->graph);
       e = le != cudaSuccess ? le : ee;
