@@ -66,7 +66,7 @@ typedef enum {
   NF4_ERR_UNSUPPORTED_BLOCKSIZE = 3, /* blocksize / s2_blocksize not a supported power of two */
   NF4_ERR_MISALIGNED = 4,            /* pointer not aligned to its element size */
   NF4_ERR_UNSUPPORTED_DTYPE = 5,     /* output type not accepted by the call */
-  NF4_ERR_UNSUPPORTED_BATCH = 6,     /* GEMV batch outside 1..8 */
+  NF4_ERR_UNSUPPORTED_BATCH = 6,     /* GEMV batch outside 1..64 */
   NF4_ERR_CUDA = 7,                  /* a CUDA runtime call failed */
   NF4_ERR_WORKSPACE = 8              /* workspace missing or too small */
 } nf4_status;
@@ -134,7 +134,8 @@ NF4_API nf4_status nf4_dequant(const uint8_t* packed, const uint8_t* absmax_q,
  *                (element (r, k) is flat index r*K + k).
  *   N, K         output and input features; N >= 0, K >= 0 and even.
  *   x            bfloat16 bit patterns [batch][K], 2-byte aligned.
- *   batch        1 .. 8 activation vectors.
+ *   batch        1 .. 64 activation vectors (above 8 they run in slabs of
+ *                up to 8, one launch each).
  *   y            binary32 [batch][N], 4-byte aligned:
  *                y[b][r] = sum_k W_hat[r][k] * x[b][k], with W_hat[r][k] the
  *                binary32 dequantized weight (before 16-bit rounding) and

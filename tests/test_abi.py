@@ -88,7 +88,7 @@ def test_gemv_argument_errors(lib):
     assert gv(lib, K=63) == ERR_SIZE
     assert gv(lib, N=1 << 30, K=1 << 12) == ERR_SIZE
     assert gv(lib, bs=96) == ERR_BS
-    for b in (0, 9, -1):
+    for b in (0, 65, -1):
         assert gv(lib, batch=b) == ERR_BATCH, b
     assert gv(lib, N=0, y=0, x=0) == OK
     assert gv(lib, y=0) == ERR_NULL
@@ -105,7 +105,7 @@ def test_gemv_ex_argument_errors(lib):
     for d in (3, -1, 7):
         assert gx(dtype=d) == ERR_DTYPE, d
     assert gx(N=-1, dtype=3) == ERR_SIZE  # sizes are checked first
-    assert gx(batch=9) == ERR_BATCH
+    assert gx(batch=65) == ERR_BATCH
     assert gx(N=0, y=0, x=0, dtype=2) == OK
     assert gx(y=0) == ERR_NULL
     assert gx(x=0, bias=A) == ERR_NULL
@@ -207,7 +207,7 @@ def test_step_argument_errors(lib):
     assert create([node(N=48), node(K=64, inp=0)]) == ERR_SIZE      # K != N of the input
     assert create([node(), node(K=32, inp=0, y=0)]) == ERR_NULL
     assert create([node(), node(K=32, inp=0, dtype=5)]) == ERR_DTYPE
-    assert create([node()], batch=9) == ERR_BATCH
+    assert create([node()], batch=65) == ERR_BATCH
     assert create([node()], x=0) == ERR_NULL
     assert create([node(y=A + 1)]) == ERR_ALIGN
     assert create([node(K=63)]) == ERR_SIZE

@@ -105,3 +105,32 @@ def test_f32_without_bias_is_nf4_gemv():
         y_ref, s_abs = oracle.gemv(t, N, K, x)
         assert_gemv_close(y0, y_ref, s_abs)
 
+
+
+@pytest.mark.parametrize("batch", [9, 16, 33, 64])
+def test_wide_batches(batch):
+    """Batches above 8 run in slabs of eight vectors (every output type, with
+    and without bias)."""
+    N, K = 37, 1536
+    t = _quantized(870 + batch, N, K, 0.001)
+    d = to_device(t)
+    x = synth.activations(880 + batch, batch, K)
+    y_ref, s_abs = oracle.gemv(t, N, K, x)
+    for name, dt in DTYPES.items():
+        b = synth.bias(890, N, name)
+        y = gpu_gemv_ex(t, N, K, x, dt, b, d=d)
+        assert_layer_close(y, y_ref, s_abs, dt, b, f"batch={batch} {name} + bias")
+    y = gpu_gemv(t, N, K, x, d=d)
+    assert_gemv_close(y, y_ref, s_abs, f"batch={batch} fp32")
+
+
+@pytest.mark.parametrize("layer", synth.LLAMA_7B_LAYERS, ids=lambda l: l.name)
+def test_llama_layers_batch_64_sampled_rows(layer):
+    """Full-size 7B layers at batch 64, checked on 192 sampled rows."""
+    t = _quantized(layer.seed, layer.N, layer.K)
+    x = synth.activations(synth.llama_x_seed(64), 64, layer.K)
+    y = gpu_gemv(t, layer.N, layer.K, x)
+    rows = np.sort(np.random.default_rng(layer.seed).choice(layer.N, 192, replace=False))
+    rows[0], rows[-1] = 0, layer.N - 1
+    y_ref, s_abs = oracle.gemv(t, layer.N, layer.K, x, rows=rows)
+    assert_gemv_close(y[:, rows], y_ref, s_abs, f"{layer.name} batch 64")

@@ -72,7 +72,7 @@ const char* nf4_status_string(nf4_status status) {
     case NF4_ERR_UNSUPPORTED_DTYPE:
       return "NF4_ERR_UNSUPPORTED_DTYPE: dequant output must be NF4_BF16 or NF4_FP16, "
              "GEMV output NF4_BF16, NF4_FP16 or NF4_F32";
-    case NF4_ERR_UNSUPPORTED_BATCH: return "NF4_ERR_UNSUPPORTED_BATCH: batch must be 1..8";
+    case NF4_ERR_UNSUPPORTED_BATCH: return "NF4_ERR_UNSUPPORTED_BATCH: batch must be 1..64";
     case NF4_ERR_CUDA: return "NF4_ERR_CUDA: a CUDA runtime call failed (see nf4_last_cuda_error)";
     case NF4_ERR_WORKSPACE: return "NF4_ERR_WORKSPACE: workspace missing or too small";
   }
@@ -119,7 +119,7 @@ nf4_status check_gemv_args(const uint8_t* packed, const uint8_t* absmax_q,
   int lbs = 0, ls2 = 0;
   nf4_status st = check_block_sizes(blocksize, s2_blocksize, &lbs, &ls2);
   if (st != NF4_OK) return st;
-  if (batch < 1 || batch > 8) return NF4_ERR_UNSUPPORTED_BATCH;
+  if (batch < 1 || batch > 64) return NF4_ERR_UNSUPPORTED_BATCH;
   if (y_dtype != NF4_BF16 && y_dtype != NF4_FP16 && y_dtype != NF4_F32)
     return NF4_ERR_UNSUPPORTED_DTYPE;
   if (N == 0) return NF4_OK;

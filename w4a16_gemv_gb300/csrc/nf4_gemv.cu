@@ -406,6 +406,20 @@ cudaError_t read_and_clear_device_flags(unsigned int* flags) {
 
 cudaError_t launch_gemv(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x, int batch,
                         const YOut& y, cudaStream_t stream) {
+  if (batch > 8) {
+    // Wider batches run as slabs of up to eight vectors, one launch each;
+    // after the first slab the weights come from L2.
+    const size_t esize = y.dtype == NF4_F32 ? 4 : 2;
+    for (int b0 = 0; b0 < batch; b0 += 8) {
+      const int nb = batch - b0 < 8 ? batch - b0 : 8;
+      YOut ys = y;
+      ys.y = static_cast<unsigned char*>(y.y) + size_t(b0) * size_t(N) * esize;
+      const cudaError_t e =
+          launch_gemv(t, N, K, x == nullptr ? nullptr : x + int64_t(b0) * K, nb, ys, stream);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
   switch (batch) {
     case 1: return dispatch_batch<1>(t, N, K, x, y, stream);
     case 2: return dispatch_batch<2>(t, N, K, x, y, stream);
