@@ -215,11 +215,14 @@ typedef struct nf4_step_st* nf4_step_t;
 /*
  * nf4_step_create -- validate the nodes (each as nf4_gemv_ex would, plus the
  * input rules above) and record them into a CUDA graph on the current
- * device. All pointers (weights, x [batch][K], biases, every y) are device
- * pointers captured by value: they must stay valid, and their contents are
- * read / written at each nf4_step_launch, not at creation. Nothing is
- * launched here. The step owns only host-side graph objects (the library
- * allocates no device buffers); free them with nf4_step_destroy.
+ * device. Consecutive nodes with the same input, K and block sizes (up to
+ * four, e.g. q/k/v or gate/up) share one launch. All pointers (weights,
+ * x [batch][K], biases, every y) are device pointers captured by value: they
+ * must stay valid, and their contents are read / written at each
+ * nf4_step_launch, not at creation. Nothing is launched here.
+ * Each node group is one kernel launch, with programmatic dependent launch
+ * between consecutive kernels. The step owns only host-side graph objects
+ * (the library allocates no device buffers). Free it with nf4_step_destroy.
  * Errors: NF4_ERR_NULL (step, nodes, or a node's pointers),
  *   NF4_ERR_INVALID_SIZE (n_nodes < 1, a bad input index, K != N of the
  *   input node, or a node's sizes), NF4_ERR_UNSUPPORTED_DTYPE (an input node

@@ -1,10 +1,10 @@
 """GPU tests of the decode step (nf4_step_create / nf4_step_launch): a
 recorded sequence of fused GEMVs, each node's input the step's x or an
-earlier node's bf16 output.
+earlier node's bf16 output, one kernel per node group.
 
-* Parity: a chain of layers against the oracle, with an error bound carried
-  through the chain (each layer's tolerance plus how far its input may be
-  from the oracle's input); every intermediate output is checked.
+* Parity: chains and decoder-shaped graphs of layers against the oracle,
+  with an error bound carried along every edge (each layer's tolerance plus
+  how far its input may be from the oracle's input); every output is checked.
 * Mechanism: replays write exactly what the same nodes launched one by one
   write, for new inputs written between replays.
 """
@@ -39,36 +39,40 @@ def _round_all(v: np.ndarray, dtype: int) -> np.ndarray:
     return np.vectorize(lambda a: oracle.round_f64(a, dtype), otypes=[np.uint32])(v)
 
 
-# (N, K, y dtype, bias) of a chain: q_proj -> o_proj -> gate_proj -> down_proj
-# shapes of a Qwen2.5-1.5B-sized decoder layer, each feeding the next.
-CHAIN = [(1536, 1536, BF16, True), (1536, 1536, BF16, False), (8960, 1536, BF16, True),
-         (1536, 8960, F32, True)]
-
-
-@pytest.mark.parametrize("batch", [1, 4])
-def test_chain_parity_with_carried_error_bound(batch):
+def _check_dag(spec, batch, seed):
+    """spec: list of (N, K, y dtype, has_bias, input) nodes. Builds the step
+    from oracle-quantized weights, runs it once and checks every node's
+    output against the oracle with the carried error bound:
+    for a node with oracle input x_or and input bound e (|x_gpu - x_or| <= e),
+    v = W x_or + bias, P = sum |w_hat| e, D = 1e-3 (sum |w_hat x_or| + P +
+    |bias|) + 1e-6 + P; the GPU output lies in [round(v - D), round(v + D)];
+    the node's own output bound is the distance from round(v) to those ends."""
     import w4a16_gemv_gb300 as nf4
     ts, nodes, biases = [], [], []
-    for i, (N, K, dt, has_bias) in enumerate(CHAIN):
-        t = oracle.quantize(synth.weights(200 + i, N * K), 64, 256, synth.code2_linear())
+    for i, (N, K, dt, has_bias, inp) in enumerate(spec):
+        t = oracle.quantize(synth.weights(seed + i, N * K), 64, 256, synth.code2_linear())
         ts.append(t)
         name = {BF16: "bf16", FP16: "fp16", F32: "f32"}[dt]
-        b = synth.bias(210 + i, N, name) if has_bias else None
+        b = synth.bias(seed + 50 + i, N, name) if has_bias else None
         biases.append(b)
         bt = None
         if b is not None:
             bt = torch.from_numpy(b.view(np.int32 if dt == F32 else np.int16)).to(dev()).view(_TDT[dt])
-        y = torch.empty((batch, N), dtype=_TDT[dt], device=dev())
-        nodes.append(dict(weight=_weight(t, N, K), y=y, bias=bt, input=i - 1))
-    x_bits = synth.activations(220 + batch, batch, CHAIN[0][1])
+        y = torch.full((batch, N), float("nan"), dtype=_TDT[dt], device=dev())
+        nodes.append(dict(weight=_weight(t, N, K), y=y, bias=bt, input=inp))
+    x_bits = synth.activations(seed + 99, batch, spec[0][1])
     x = u16_to_torch(x_bits, torch.bfloat16).view(batch, -1)
     step = nf4.DecodeStep(nodes, x)
     step.launch()
     torch.cuda.synchronize()
+    assert nf4.nf4_device_error_flags() == 0
 
-    x_or = x_bits                              # the oracle's input to the current layer
-    e = np.zeros((batch, CHAIN[0][1]))         # how far the GPU's input may be from it
-    for i, (N, K, dt, _) in enumerate(CHAIN):
+    outs = {}                                  # node -> (oracle output bits, bound)
+    for i, (N, K, dt, _, inp) in enumerate(spec):
+        if inp == -1:
+            x_or, e = x_bits, np.zeros((batch, K))
+        else:
+            x_or, e = outs[inp]
         y_ref, s_abs = oracle.gemv(ts[i], N, K, x_or)
         p = oracle.gemv_abs(ts[i], N, K, e)
         v, y_or = oracle.gemv_output(y_ref, dt, biases[i])
@@ -78,10 +82,48 @@ def test_chain_parity_with_carried_error_bound(batch):
         y = decode_bits(_bits(nodes[i]["y"]), dt)
         bad = ~((decode_bits(lo, dt) <= y) & (y <= decode_bits(hi, dt)))
         assert not bad.any(), f"node {i}: {bad.sum()} outputs outside the carried bound"
-        x_or = y_or.astype(np.uint16)
         c = decode_bits(y_or, dt)
-        e = np.maximum(decode_bits(hi, dt) - c, c - decode_bits(lo, dt))
+        outs[i] = (y_or.astype(np.uint16), np.maximum(decode_bits(hi, dt) - c, c - decode_bits(lo, dt)))
     step.close()
+
+
+# q_proj -> o_proj -> gate_proj -> down_proj shapes of a Qwen2.5-1.5B-sized
+# decoder layer, each feeding the next (the last in binary32).
+CHAIN = [(1536, 1536, BF16, True, -1), (1536, 1536, BF16, False, 0), (8960, 1536, BF16, True, 1),
+         (1536, 8960, F32, True, 2)]
+
+
+@pytest.mark.parametrize("batch", [1, 4])
+def test_chain_parity_with_carried_error_bound(batch):
+    _check_dag(CHAIN, batch, 200)
+
+
+def _small_decoder(layers, h=512, kv=128, inter=1536):
+    """Decoder-shaped node graph at reduced width: q, k, v from the layer
+    input; o from q; gate, up from o; down from gate; next layer from down."""
+    spec = []
+    for layer in range(layers):
+        base = 7 * layer
+        inp = -1 if layer == 0 else base - 1
+        spec += [(h, h, BF16, True, inp), (kv, h, BF16, True, inp), (kv, h, FP16, True, inp),
+                 (h, h, BF16, False, base), (inter, h, BF16, False, base + 3),
+                 (inter, h, F32, False, base + 3), (h, inter, BF16, False, base + 4)]
+    return spec
+
+
+@pytest.mark.parametrize("batch", [1, 2])
+def test_decoder_graph_parity(batch):
+    """Two decoder layers: eight launches (q/k/v and gate/up grouped)."""
+    _check_dag(_small_decoder(2), batch, 260)
+
+
+def test_small_and_fallback_node_groups():
+    """Groups with fewer rows than SMs, and a node (K = 40, not a multiple
+    of 32) that the streaming kernels do not take (its own launch)."""
+    spec = [(64, 256, BF16, True, -1), (7, 256, BF16, False, -1), (256, 64, BF16, True, 0),
+            (2, 256, F32, False, 2), (40, 256, BF16, True, 2), (256, 40, FP16, False, 4)]
+    _check_dag(spec, 1, 290)
+    _check_dag(spec, 3, 291)
 
 
 def _decoder_nodes(layers, batch, seed):

@@ -40,6 +40,54 @@ void destroy_graph(nf4_step_st* s) {
   s->graph = nullptr;
 }
 
+// Consecutive non-empty nodes from i that read the same input with the same
+// K and block sizes (e.g. q/k/v, gate/up), at most kMaxSub.
+int32_t group_at(const nf4_gemv_node* nodes, int32_t n_nodes, int32_t i) {
+  int32_t n = 1;
+  while (n < nf4::kMaxSub && i + n < n_nodes && nodes[i + n].N > 0 &&
+         nodes[i + n].input == nodes[i].input && nodes[i + n].K == nodes[i].K &&
+         nodes[i + n].blocksize == nodes[i].blocksize &&
+         nodes[i + n].s2_blocksize == nodes[i].s2_blocksize)
+    ++n;
+  return n;
+}
+
+// One launch per node group, in node order, with programmatic dependent
+// launch between consecutive kernels.
+cudaError_t record_nodes(const nf4_gemv_node* nodes, int32_t n_nodes, int32_t batch,
+                            const std::vector<nf4::QuantTensor>& ts,
+                            const std::vector<nf4::YOut>& outs,
+                            const std::vector<const uint16_t*>& xs, nf4_step_st* s,
+                            cudaStream_t cs) {
+  // Relaxed: first launches of a kernel may set its shared-memory limit.
+  cudaError_t e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed);
+  if (e != cudaSuccess) return e;
+  cudaError_t le = cudaSuccess;
+  for (int32_t i = 0; i < n_nodes && le == cudaSuccess;) {
+    if (nodes[i].N == 0) {
+      ++i;
+      continue;
+    }
+    int32_t n = group_at(nodes, n_nodes, i);
+    bool done = false;
+    if (n > 1 && nodes[i].K > 0) {
+      int64_t Ns[nf4::kMaxSub];
+      for (int32_t j = 0; j < n; ++j) Ns[j] = nodes[i + j].N;
+      le = nf4::launch_gemv_group(&ts[size_t(i)], Ns, &outs[size_t(i)], int(n), nodes[i].K,
+                                  xs[size_t(i)], batch, cs, &done);
+    }
+    if (!done) n = 1;
+    if (le == cudaSuccess && !done)
+      le = nf4::launch_gemv(ts[size_t(i)], nodes[i].N, nodes[i].K, xs[size_t(i)], batch,
+                            outs[size_t(i)], cs);
+    i += n;
+  }
+  const cudaError_t ee = cudaStreamEndCapture(cs, &s->graph);
+  e = le != cudaSuccess ? le : ee;
+  if (e == cudaSuccess && s->graph) e = cudaGraphInstantiate(&s->exec, s->graph, 0ull);
+  return e;
+}
+
 }  // namespace
 
 extern "C" {
@@ -82,40 +130,7 @@ nf4_status nf4_step_create(const nf4_gemv_node* nodes, int32_t n_nodes, const ui
   cudaStream_t cs = nullptr;
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
   if (e == cudaSuccess) {
-    // Relaxed: first launches of a kernel may set its shared-memory limit.
-    e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed);
-    if (e == cudaSuccess) {
-      cudaError_t le = cudaSuccess;
-      for (int32_t i = 0; i < n_nodes && le == cudaSuccess;) {
-        if (nodes[i].N == 0) {
-          ++i;
-          continue;
-        }
-        // Consecutive nodes reading the same input (e.g. q/k/v, gate/up)
-        // share one launch when the streaming kernels can take them.
-        int32_t n = 1;
-        while (n < nf4::kMaxSub && i + n < n_nodes && nodes[i + n].N > 0 &&
-               nodes[i + n].input == nodes[i].input && nodes[i + n].K == nodes[i].K &&
-               nodes[i + n].blocksize == nodes[i].blocksize &&
-               nodes[i + n].s2_blocksize == nodes[i].s2_blocksize)
-          ++n;
-        bool done = false;
-        if (n > 1 && nodes[i].K > 0) {
-          int64_t Ns[nf4::kMaxSub];
-          for (int32_t j = 0; j < n; ++j) Ns[j] = nodes[i + j].N;
-          le = nf4::launch_gemv_group(&ts[size_t(i)], Ns, &outs[size_t(i)], int(n), nodes[i].K,
-                                      xs[size_t(i)], batch, cs, &done);
-        }
-        if (!done) n = 1;
-        if (le == cudaSuccess && !done)
-          le = nf4::launch_gemv(ts[size_t(i)], nodes[i].N, nodes[i].K, xs[size_t(i)], batch,
-                                outs[size_t(i)], cs);
-        i += n;
-      }
-      const cudaError_t ee = cudaStreamEndCapture(cs, &s->graph);
-      e = le != cudaSuccess ? le : ee;
-    }
-    if (e == cudaSuccess && s->graph) e = cudaGraphInstantiate(&s->exec, s->graph, 0ull);
+    e = record_nodes(nodes, n_nodes, batch, ts, outs, xs, s, cs);
     cudaStreamDestroy(cs);
   }
   if (e != cudaSuccess) {
