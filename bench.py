@@ -492,9 +492,89 @@ def _sweep_time(launch, nsets, reps=5):
     return best
 
 
+def decode_step_qwen(dev, gen, code2, batch, layers=28):
+    """A recorded decode step (nf4_step_create) over the linear layers of a
+    Qwen2.5-1.5B-shaped decoder: per layer q/k/v (with bias) from the layer
+    input, o from q, gate/up from o, down from gate; bf16 outputs; random
+    codes and scales (timing does not depend on the values). Returns the
+    step's timer (us per replay, replays back to back on one stream), its
+    weight bytes and its kernel launches per replay (q/k/v and gate/up
+    grouped)."""
+    import torch
+
+    import w4a16_gemv_gb300 as nf4
+    shapes = [(1536, 1536), (256, 1536), (256, 1536), (1536, 1536), (8960, 1536), (8960, 1536),
+              (1536, 8960)]
+    inputs = [-1, -1, -1, 0, 3, 3, 4]
+    nodes, wbytes = [], 0
+    for layer in range(layers):
+        base = 7 * layer
+        for j, (N, K) in enumerate(shapes):
+            n = N * K
+            nb = (n + BS - 1) // BS
+            ng = (nb + S2 - 1) // S2
+            wt = nf4.NF4Weight(torch.randint(0, 256, (n // 2,), dtype=torch.uint8, device=dev, generator=gen),
+                               torch.randint(0, 256, (nb,), dtype=torch.uint8, device=dev, generator=gen),
+                               (torch.rand(ng, device=dev, generator=gen) * 0.04 + 0.01).half(),
+                               code2, 0.01, n, (N, K), BS, S2)
+            wbytes += n // 2 + nb + 2 * ng
+            inp = inputs[j]
+            inp = (-1 if layer == 0 else base - 1) if inp == -1 else base + inp
+            bias = torch.randn(N, device=dev, generator=gen).to(torch.bfloat16) if j < 3 else None
+            nodes.append(dict(weight=wt, y=torch.empty((batch, N), dtype=torch.bfloat16, device=dev),
+                              bias=bias, input=inp))
+    x = torch.randn((batch, 1536), device=dev, generator=gen).to(torch.bfloat16)
+    step = nf4.DecodeStep(nodes, x)
+
+    def time_step(reps=5, m=50):
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            for _ in range(5):
+                step.launch(s)
+        s.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        best = None
+        for _ in range(reps):
+            with torch.cuda.stream(s):
+                e0.record(s)
+                for _ in range(m):
+                    step.launch(s)
+                e1.record(s)
+            s.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / m
+            best = us if best is None else min(best, us)
+        return best
+    return {"time": time_step, "weight_bytes": wbytes, "launches": 4 * layers, "close": step.close}
+
+
+def run_decode_step(args):
+    """--decode-step: W replays untimed, then K replays back to back between
+    two events; one JSON line."""
+    import numpy as np
+    import torch
+    dev = torch.device("cuda:0")
+    peak, peak_kind = load_peaks()
+    code2 = torch.from_numpy((((np.arange(256) - 127.5) / 127.5).astype(np.float16))).to(dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4242)
+    step = decode_step_qwen(dev, gen, code2, args.batch)
+    us = step["time"](reps=1, m=args.steps) if args.warmup >= 0 else None
+    gbs = step["weight_bytes"] / us / 1e3
+    step["close"]()
+    return {"metric": "decode step us (Qwen2.5-1.5B-shaped, 28 layers x 7 fused GEMVs)",
+            "value": round(us, 1), "unit": "us/step", "higher_is_better": False,
+            "batch": args.batch, "steps": args.steps, "launches_per_step": step["launches"],
+            "weight_bytes": step["weight_bytes"], "gbs": round(gbs, 1),
+            "frac_of_measured_hbm": round(gbs / peak, 4), "peak_kind": peak_kind,
+            "data": "synthetic random codes and scales; weights 676 MB > L2 (no flush needed)"}
+
+
 def run_sweep(args):
     """Times nf4_dequant on configs 0, 1, 2 (standalone dequant of each Qwen
-    layer) and 4, and nf4_gemv on configs 2 and 3 at batch 1/4/8. Inputs are
+    layer) and 4, nf4_gemv on configs 2 and 3 at batch 1/4/8, nf4_gemv_ex
+    (bf16 y + bias), batches 16/32/64 on config 3, and the recorded decode
+    step of a Qwen2.5-1.5B-shaped decoder at batch 1 and 4. Inputs are
     synthetic random codes and scales (timing does not depend on the values);
     each case rotates over enough input sets to exceed 4x the L2."""
     import ctypes
@@ -587,7 +667,66 @@ def run_sweep(args):
                         "sets": r})
             del sets
             torch.cuda.empty_cache()
+    # Output stage fused (bf16 y + bias) and batches above 8 (slabs of eight).
+    ex_cases = [("cfg2 q/o bf16+bias", 1536, 1536, 1), ("cfg2 k/v bf16+bias", 256, 1536, 1),
+                ("cfg3 attn bf16+bias", 4096, 4096, 1)]
+    ex_cases += [(f"cfg3 {nm} wide", N, K, b) for nm, N, K in
+                 (("attn", 4096, 4096), ("gate/up", 11008, 4096), ("down", 4096, 11008))
+                 for b in (16, 32, 64)]
+    for name, N, K, batch in ex_cases:
+        n = N * K
+        nb = (n + BS - 1) // BS
+        ng = (nb + S2 - 1) // S2
+        ex = "bias" in name
+        bytes_ = n // 2 + nb + 2 * ng + 512 + 2 * batch * K + (2 if ex else 4) * batch * N + (2 * N if ex else 0)
+        r = max(2, nsets_for(bytes_))
+        sets = []
+        for _ in range(r):
+            st = quant_set(n)
+            st["x"] = torch.randn(batch, K, device=dev, generator=gen).to(torch.bfloat16)
+            st["y"] = torch.empty(batch, N, device=dev, dtype=torch.bfloat16 if ex else torch.float32)
+            st["b"] = torch.randn(N, device=dev, generator=gen).to(torch.bfloat16)
+            sets.append(st)
+
+        def launch(i, sp, N=N, K=K, batch=batch, sets=sets, ex=ex):
+            st = sets[i]
+            if ex:
+                rc = lib.nf4_gemv_ex(st["packed"].data_ptr(), st["absmax_q"].data_ptr(),
+                                     st["absmax2"].data_ptr(), code2.data_ptr(), 0.01, N, K, BS, S2,
+                                     st["x"].data_ptr(), batch, st["b"].data_ptr(), st["y"].data_ptr(),
+                                     0, sp)
+            else:
+                rc = lib.nf4_gemv(st["packed"].data_ptr(), st["absmax_q"].data_ptr(),
+                                  st["absmax2"].data_ptr(), code2.data_ptr(), 0.01, N, K, BS, S2,
+                                  st["x"].data_ptr(), batch, st["y"].data_ptr(), sp)
+            if rc != 0:
+                raise RuntimeError(f"nf4_gemv: {nf4.nf4_status_string(rc)}")
+        us = _sweep_time(launch, r)
+        gbs = bytes_ / us / 1e3
+        out.append({"kind": "gemv", "case": name, "N": N, "K": K, "batch": batch, "bytes": bytes_,
+                    "us_per_layer": round(us, 3), "gbs": round(gbs, 1),
+                    "frac_of_measured_hbm": round(gbs / peak, 4), "frac_of_8000": round(gbs / 8000.0, 4),
+                    "sets": r})
+        del sets
+        torch.cuda.empty_cache()
+
+    for batch in (1, 4):
+        step = decode_step_qwen(dev, gen, code2, batch)
+        us, wbytes = step["time"](), step["weight_bytes"]
+        gbs = wbytes / us / 1e3
+        out.append({"kind": "decode_step", "case": "Qwen2.5-1.5B-shaped step, 28 layers x 7 GEMVs",
+                    "batch": batch, "launches": step["launches"], "weight_bytes": wbytes,
+                    "us_per_step": round(us, 1), "gbs": round(gbs, 1),
+                    "frac_of_measured_hbm": round(gbs / peak, 4)})
+        step["close"]()
+        torch.cuda.empty_cache()
+
     for d in out:
+        if d["kind"] == "decode_step":
+            print(f"{'step':8s} {d['case'] + ' B=' + str(d['batch']):44s} {d['us_per_step']:10.1f} us "
+                  f"{d['gbs']:9.1f} GB/s {100 * d['frac_of_measured_hbm']:5.1f}% of {peak:.0f} ({peak_kind})",
+                  file=sys.stderr)
+            continue
         what = d["case"] + (f" {d['out']}" if d["kind"] == "dequant" else f" B={d['batch']}")
         t = d["us"] if d["kind"] == "dequant" else d["us_per_layer"]
         print(f"{d['kind']:8s} {what:44s} {t:10.3f} us {d['gbs']:9.1f} GB/s "
@@ -610,6 +749,9 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--sweep", action="store_true",
                     help="time every dequant and GEMV configuration instead of the step")
+    ap.add_argument("--decode-step", action="store_true",
+                    help="time the recorded decode step of a Qwen2.5-1.5B-shaped decoder instead")
+    ap.add_argument("--batch", type=int, default=1, help="batch of --decode-step")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -628,6 +770,10 @@ def main():
     if args.sweep:
         if rank == 0:
             print(json.dumps(run_sweep(args)), flush=True)
+        return
+    if args.decode_step:
+        if rank == 0:
+            print(json.dumps(run_decode_step(args)), flush=True)
         return
 
     if world > 1:
