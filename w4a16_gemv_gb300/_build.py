@@ -13,7 +13,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libnf4.so")
 SOURCES = ("nf4_api.cu", "nf4_dequant.cu", "nf4_gemv.cu", "nf4_gemv_stream.cu", "nf4_quantize.cu",
-           "nf4_step.cu")
+           "nf4_step.cu", "nf4_gemm_tc.cu")
 GENCODE = "arch=compute_103a,code=sm_103a"
 
 

@@ -1,0 +1,583 @@
+// nf4_gemm_tc.cu -- the fused GEMV for wide batches (16..64 vectors) on the
+// 5th-generation tensor cores: y = W_hat x with the dequantization fused.
+//
+// At these batches the contraction is dense ("CUDA 进阶手册 / 量化与 GEMV",
+// exercise on batch 1/4/32/128: past a few vectors the weights are reused
+// enough that the W4A16 path moves to FP16 tensor cores); CUDA-core FMAs
+// would make it compute-bound. Per CTA, a tile of 128 weight rows:
+//   * the stage's packed weight tile (128 rows x 32 bytes) and x tile go
+//     through 8-deep rings in shared memory filled by 2-D tensor copies (TMA;
+//     x 128-byte swizzled; rows past the weight or the batch zero-filled)
+//     that complete on mbarriers;
+//   * sixteen producer warps dequantize in registers: w_hat = fp32(NF4[idx] *
+//     s) exactly as the dequantization defines it, split into bfloat16 hi =
+//     rn(w_hat) and lo = rn(w_hat - hi) (the residual is exact, so w_hat is
+//     represented to about 2^-17 relative), and store both into tensor memory
+//     (TMEM lane = weight row) -- the A operand never touches shared memory;
+//   * x stays bfloat16 (exact) in shared memory as the B operand, 128-byte
+//     swizzled, K-major;
+//   * one warp issues tcgen05.mma (kind::f16, bf16 x bf16 -> fp32 in TMEM),
+//     two per 16-element K step (hi and lo), once the producer warps have
+//     signalled the stage's A buffer full; its commits free the A buffer and
+//     the ring slot, which another warp refills with the tile copies. The producers run
+//     up to four stages ahead of the MMAs (four A buffers in TMEM);
+//   * K is split over a thread-block cluster; partial sums are added in rank
+//     order through distributed shared memory (deterministic) and the output
+//     stage (bias, rounding to y's type) is applied once.
+// Every wait on an mbarrier is bounded (about one second); a wait that runs
+// out sets bit 0 of the device error flags and the kernel still completes
+// its cluster barriers and frees its tensor memory.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+
+#include "nf4_internal.cuh"
+
+namespace nf4 {
+namespace {
+
+constexpr int kProducerWarps = 16;  // warp w < 16: rows 32 * (w % 4) + lane, K quarter w / 4
+constexpr int kMmaWarp = kProducerWarps;       // issues the MMAs
+constexpr int kCopyWarp = kProducerWarps + 1;  // starts the tile copies
+constexpr int kTcThreads = 32 * (kProducerWarps + 2);
+constexpr int kTileM = 128;
+constexpr int kStageK = 64;      // elements of K per stage
+constexpr int kRing = 8;         // stages of packed weights and x in shared memory
+constexpr int kAhead = kRing - 2;  // stages loaded ahead of the one being dequantized
+constexpr int kMaxStagesPerCta = 64;
+constexpr int kNA = 4;               // A buffers in TMEM (the producers' lead over the MMAs)
+constexpr uint32_t kTmemCols = 512;  // A: kNA buffers x 64 columns (hi 32 + lo 32); D: 256..319
+
+__device__ unsigned int g_tc_flags = 0;  // bit 0: an mbarrier wait ran out
+
+struct TcArgs {
+  QuantTensor t;
+  YOut out;
+  const uint16_t* x;
+  int64_t N;
+  int32_t K;
+  int batch;
+  int splits;  // CTAs per cluster, along K (1, 2, 4 or 8)
+  uint32_t off_b, off_w, off_scale, off_tab, off_c2, off_bar;
+};
+
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart (the leading-byte offset is not used by this layout).
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+  return uint64_t((saddr >> 4) & 0x3FFFu) | (uint64_t(1) << 16) | (uint64_t(1024 >> 4) << 32) |
+         (uint64_t(1) << 46) | (uint64_t(2) << 61);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, M = 128, N = bn.
+__host__ __device__ constexpr uint32_t idesc_bf16(int bn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(bn >> 3) << 17) | (uint32_t(kTileM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t (&v)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+               : "r"(taddr)
+               : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t local_addr, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+// Packed binary32 multiply and subtract (two independent IEEE operations,
+// round to nearest).
+__device__ __forceinline__ float2 fmul2_rn(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 fsub2_rn(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "sub.rn.f32x2 rd, ra, rb;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_rn(float2 v) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(v.y), "f"(v.x));  // element 0 low
+  return r;
+}
+__device__ __forceinline__ float2 bf16x2_to_f2(uint32_t v) {
+  return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    gemm_tc_kernel(const TcArgs p, const __grid_constant__ CUtensorMap tmx,
+                   const __grid_constant__ CUtensorMap tmw) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  // tile copies and the swizzled x layout want a 1024-byte aligned base (the
+  // host allocates 1024 bytes of slack)
+  unsigned char* const smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int kq = warp >> 2;                 // K quarter of a stage (16 elements)
+  const int row = (warp & 3) * 32 + lane;   // row of the tile = TMEM lane
+  const int tile = int(blockIdx.x) / p.splits;
+  const int split = int(blockIdx.x) - tile * p.splits;  // rank in the cluster
+  const int64_t r_glob = int64_t(tile) * kTileM + row;
+  const bool row_ok = r_glob < p.N;
+  const QuantTensor& t = p.t;
+  const int64_t K = p.K;
+  const int S = int(K / kStageK);
+  const int s0 = int(int64_t(split) * S / p.splits);
+  const int ns = int(int64_t(split + 1) * S / p.splits) - s0;
+
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t b_ring = sbase + p.off_b;                    // kRing slots of BN x 128 B
+  const uint32_t w_ring = sbase + p.off_w;                    // kRing slots of 4 KB
+  float* sScale = reinterpret_cast<float*>(smem + p.off_scale);  // [stage][128]
+  float* sC2 = reinterpret_cast<float*>(smem + p.off_c2);
+  uint64_t* afull = reinterpret_cast<uint64_t*>(smem + p.off_bar);  // A buffer written (16 warps)
+  uint64_t* aempty = afull + kNA;  // MMAs of the A buffer done
+  uint64_t* xfull = afull + 2 * kNA;  // x tile landed, per slot
+  uint64_t* xempty = xfull + kRing;  // MMAs reading the x slot done
+  uint64_t* wfull = xempty + kRing;  // weight tile landed, per slot
+  uint32_t* s_taddr = reinterpret_cast<uint32_t*>(smem + p.off_bar + 8 * (2 * kNA + 3 * kRing));
+  float* red = reinterpret_cast<float*>(smem + p.off_b);     // [BN][128] after the main loop
+
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(s_taddr)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (tid == 0) {
+    for (int i = 0; i < kNA; ++i) {
+      mbar_init(&afull[i], kProducerWarps);
+      mbar_init(&aempty[i], 1);
+    }
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(&xfull[i], 1);
+      mbar_init(&xempty[i], 1);
+      mbar_init(&wfull[i], 1);
+    }
+    fence_mbar_init();
+  }
+
+  const bool producer = warp < kProducerWarps;
+  // Small inputs first (their latency hides behind the table build): the
+  // code2 entry of this thread, and the absmax_q / absmax2 of this row for
+  // its first stages (stages i = kq mod 4; the rest below if more than 32).
+  const uint16_t c2v = tid < 256 ? __ldg(t.code2 + tid) : uint16_t(0);
+  uint8_t q0[8];
+  uint16_t a20[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int i = kq + 4 * u;
+    q0[u] = 0;
+    a20[u] = 0;
+    if (producer && i < ns && row_ok) {
+      const int64_t blk = (r_glob * K + int64_t(s0 + i) * kStageK) >> t.lbs;
+      q0[u] = __ldg(t.absmax_q + blk);
+      a20[u] = __ldg(t.absmax2 + (blk >> t.ls2));
+    }
+  }
+  // The weight and x tiles of stage i into ring slot i % kRing (thread
+  // kTcThreads - 32 only).
+  auto issue_tiles = [&](int i) {
+    const int slot = i % kRing;
+    mbar_arrive_expect_tx(&wfull[slot], uint32_t(kTileM * kStageK / 2));
+    tma_load_2d(w_ring + uint32_t(slot) * 4096u, &tmw, (s0 + i) * (kStageK / 2), tile * kTileM,
+                &wfull[slot]);
+    mbar_arrive_expect_tx(&xfull[slot], uint32_t(BN * 128));
+    tma_load_2d(b_ring + uint32_t(slot) * uint32_t(BN * 128), &tmx, (s0 + i) * kStageK, 0, &xfull[slot]);
+  };
+  __syncthreads();  // barriers initialised before any copy uses one
+  if (warp == kCopyWarp && lane == 0)
+    for (int i = 0; i < kAhead && i < ns; ++i) issue_tiles(i);
+
+  // Lane-private pair table: row e (256 B) holds (NF4[e >> 4], NF4[e & 15])
+  // for lane l at bytes 8l..8l+7 (no bank conflicts).
+  {
+    const float my_code = nf4_code_select(lane & 15);
+    unsigned char* tabp = smem + p.off_tab;
+    for (int i = tid; i < 256 * 16; i += kTcThreads) {
+      const int e = i >> 4, q = i & 15;
+      const float hi = __shfl_sync(0xffffffffu, my_code, e >> 4);
+      const float lo = __shfl_sync(0xffffffffu, my_code, e & 15);
+      *reinterpret_cast<float4*>(tabp + e * 256 + q * 16) = make_float4(hi, lo, hi, lo);
+    }
+  }
+  if (tid < 256) sC2[tid] = half_bits_to_float(c2v);
+  __syncthreads();  // sC2 ready
+
+  // Block scales of this thread's row for the CTA's stages (stages i = kq
+  // mod 4): fp32(fp32(code2[q] * absmax2[g]) + offset); 0 past the last row.
+  for (int i0 = kq; producer && i0 < ns; i0 += 32) {
+    uint8_t q[8];
+    uint16_t a2[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + 4 * u;
+      q[u] = q0[u];
+      a2[u] = a20[u];
+      if (i0 != kq && i < ns && row_ok) {
+        const int64_t blk = (r_glob * K + int64_t(s0 + i) * kStageK) >> t.lbs;
+        q[u] = __ldg(t.absmax_q + blk);
+        a2[u] = __ldg(t.absmax2 + (blk >> t.ls2));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + 4 * u;
+      if (i < ns)
+        sScale[i * kTileM + row] =
+            row_ok ? __fadd_rn(__fmul_rn(sC2[q[u]], half_bits_to_float(a2[u])), t.offset) : 0.0f;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *s_taddr;
+  const uint32_t lane_base = tbase + (uint32_t((warp & 3) * 32) << 16);
+  const uint32_t d_col = tbase + 64u * kNA;
+  const uint32_t tab_lane = sbase + p.off_tab + (uint32_t(lane) << 3);
+  constexpr uint32_t kIdesc = idesc_bf16(BN);
+  bool ok = true;
+
+  if (producer) {
+#pragma unroll 1
+    for (int i = 0; i < ns; ++i) {
+      const int buf = i % kNA;
+      if (i >= kNA) {  // the MMAs of stage i - kNA have read A buffer `buf`
+        ok = mbar_wait_bounded(&aempty[buf], uint32_t(((i - kNA) / kNA) & 1), kWaitLimitCycles) && ok;
+        tc_fence_after();
+      }
+      ok = mbar_wait_bounded(&wfull[i % kRing], uint32_t((i / kRing) & 1), kWaitLimitCycles) && ok;
+
+      // dequantize 16 elements (8 packed bytes) of this row: w_hat = fp32(NF4
+      // code * s), split into bfloat16 hi + lo (scale 0 past the last row)
+      const float sc = sScale[i * kTileM + row];
+      const float2 sc2 = make_float2(sc, sc);
+      uint32_t wd0, wd1;
+      asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];"
+                   : "=r"(wd0), "=r"(wd1)
+                   : "r"(w_ring + uint32_t(i % kRing) * 4096u + uint32_t(row) * 32u + uint32_t(kq) * 8u));
+      uint32_t hi[8], lo[8];
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        const uint32_t word = b < 4 ? wd0 : wd1;
+        const uint32_t addr = tab_lane + (__byte_perm(word, 0u, 0x4440u + uint32_t(b & 3)) << 8);
+        float2 c;
+        asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(c.x), "=f"(c.y) : "r"(addr));
+        const float2 w = fmul2_rn(c, sc2);
+        hi[b] = bf16x2_rn(w);
+        lo[b] = bf16x2_rn(fsub2_rn(w, bf16x2_to_f2(hi[b])));  // exact residual
+      }
+      const uint32_t acol = lane_base + uint32_t(buf) * 64u + uint32_t(kq) * 8u;
+      tmem_st8(acol, hi);
+      tmem_st8(acol + 32u, lo);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&afull[buf]);
+    }
+  } else if (warp == kMmaWarp && lane == 0) {
+    // MMA issue. One thread, sharing its scheduler with producer warps: the
+    // per-stage instruction stream is kept short (ring and buffer indices
+    // and phases advance incrementally; the x-tile descriptor of a slot and
+    // K step is the slot-0 descriptor plus a constant in its 16-byte address
+    // field).
+    const uint64_t desc0 = desc_sw128(b_ring);
+    constexpr uint32_t kSlotUnits = uint32_t(BN * 128) >> 4;
+    uint32_t slot = 0, slot_ph = 0, abuf = 0, a_ph = 0;
+#pragma unroll 1
+    for (int i = 0; i < ns; ++i) {
+      ok = mbar_wait_bounded(&afull[abuf], a_ph, kWaitLimitCycles) && ok;
+      ok = mbar_wait_bounded(&xfull[slot], slot_ph, kWaitLimitCycles) && ok;
+      tc_fence_after();
+      const uint32_t a_t = tbase + abuf * 64u;
+      const uint64_t bd = desc0 + uint64_t(slot * kSlotUnits);
+      mma_bf16(d_col, a_t, bd, kIdesc, i > 0 ? 1u : 0u);
+      mma_bf16(d_col, a_t + 32u, bd, kIdesc, 1u);
+#pragma unroll
+      for (int j = 1; j < kStageK / 16; ++j) {  // 32 bytes of K per step
+        mma_bf16(d_col, a_t + 8u * uint32_t(j), bd + uint64_t(2 * j), kIdesc, 1u);
+        mma_bf16(d_col, a_t + 32u + 8u * uint32_t(j), bd + uint64_t(2 * j), kIdesc, 1u);
+      }
+      tc_commit(&aempty[abuf]);
+      tc_commit(&xempty[slot]);
+      if (++abuf == uint32_t(kNA)) {
+        abuf = 0;
+        a_ph ^= 1u;
+      }
+      if (++slot == uint32_t(kRing)) {
+        slot = 0;
+        slot_ph ^= 1u;
+      }
+    }
+  } else if (warp == kCopyWarp && lane == 0) {
+    // Tile copies of stage nx into the slot of stage nx - kRing once that
+    // stage's MMAs are done (its weight tile was consumed before the
+    // producers signalled it).
+#pragma unroll 1
+    for (int nx = kAhead; nx < ns; ++nx) {
+      if (nx >= kRing)
+        ok = mbar_wait_bounded(&xempty[nx & (kRing - 1)], uint32_t(((nx >> 3) + 1) & 1), kWaitLimitCycles) && ok;
+      issue_tiles(nx);
+    }
+  }
+  __syncwarp();
+  // all MMAs done (the last commit covers every earlier one)
+  if (ns > 0)
+    ok = mbar_wait_bounded(&aempty[(ns - 1) % kNA], uint32_t(((ns - 1) / kNA) & 1), kWaitLimitCycles) && ok;
+  tc_fence_after();
+  __syncthreads();  // the x ring is free: it becomes the partial-sum buffer
+
+  // This CTA's partial sums D[row][n] -> red[n][row]; warp (row quarter,
+  // K quarter kq) copies columns [kq * BN / 4, (kq + 1) * BN / 4).
+#pragma unroll
+  for (int c0 = 0; c0 < BN / 4 && producer; c0 += 4) {
+    uint32_t v[4];
+    tmem_ld4(lane_base + 64u * kNA + uint32_t(kq * (BN / 4) + c0), v);
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      red[(kq * (BN / 4) + c0 + j) * kTileM + row] = ok ? __uint_as_float(v[j]) : __uint_as_float(0x7fc00000u);
+  }
+  if (!ok) atomicOr(&g_tc_flags, 1u);
+  cluster_sync();  // every rank's partial sums are written
+
+  // Rows [split * 128 / splits, (split + 1) * 128 / splits) of the tile:
+  // the sum over ranks in rank order, then the output stage.
+  const int rows_per = kTileM / p.splits;
+  const int rb = split * rows_per;
+  const uint32_t red_s = smem_u32(red);
+  const int total = rows_per * p.batch;  // <= 128 * 64 / splits
+  for (int e0 = tid; e0 < total; e0 += 4 * kTcThreads) {
+    float part[4][8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {  // every load of up to four outputs in flight at once
+      const int e = e0 + u * kTcThreads;
+      const int b = e / rows_per;
+      const int r = rb + (e - b * rows_per);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        part[u][q] = (e < total && q < p.splits)
+                         ? ld_dsmem_f32(red_s + uint32_t(b * kTileM + r) * 4u, uint32_t(q))
+                         : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int e = e0 + u * kTcThreads;
+      if (e >= total) break;
+      const int b = e / rows_per;
+      const int r = rb + (e - b * rows_per);
+      const int64_t rg = int64_t(tile) * kTileM + r;
+      float v = part[u][0];
+#pragma unroll
+      for (int q = 1; q < 8; ++q)
+        if (q < p.splits) v += part[u][q];  // rank order
+      if (rg < p.N) y_store(p.out, int64_t(b) * p.N + rg, v, y_bias_bits(p.out, rg));
+    }
+  }
+  cluster_sync();  // peers are done reading this CTA's partial sums
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+// cuTensorMapEncodeTiled from the driver, looked up once.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    tried = true;
+  }
+  return fn;
+}
+
+template <int BN>
+cudaError_t launch_tc(const TcArgs& a, const CUtensorMap& tmx, const CUtensorMap& tmw, int grid,
+                      uint32_t smem, cudaStream_t stream) {
+  auto kern = gemm_tc_kernel<BN>;
+  static int attr_set[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = 1;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(grid));
+  cfg.blockDim = dim3(unsigned(kTcThreads));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = unsigned(a.splits);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a, tmx, tmw);
+}
+
+}  // namespace
+
+cudaError_t try_gemm_tc(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x, int batch,
+                        const YOut& out, int sms, cudaStream_t stream, bool* done) {
+  *done = false;
+  if (batch < 9 || batch > 64 || N <= 0 || K <= 0 || K % kStageK != 0) return cudaSuccess;
+  if (t.lbs < 6 || (K & ((int64_t(1) << t.lbs) - 1)) != 0) return cudaSuccess;  // blocksize >= 64, rows whole blocks
+  if ((reinterpret_cast<uintptr_t>(t.packed) & 15u) != 0 || (reinterpret_cast<uintptr_t>(x) & 15u) != 0)
+    return cudaSuccess;
+  const int BN = (batch + 15) / 16 * 16;
+  const int64_t tiles = (N + kTileM - 1) / kTileM;
+  const int S = int(K / kStageK);
+  if (tiles > (int64_t(1) << 24)) return cudaSuccess;
+  // K split over a cluster: fill the SMs, at most 64 stages (4096 elements)
+  // and at least 4 stages per CTA.
+  int splits = 1;
+  while (splits < 8 && (S + splits - 1) / splits > kMaxStagesPerCta) splits *= 2;
+  while (splits < 8 && tiles * splits * 2 <= sms && S / (splits * 2) >= 4) splits *= 2;
+  if ((S + splits - 1) / splits > kMaxStagesPerCta) return cudaSuccess;
+  const int grid = int(tiles) * splits;
+
+  TcArgs a;
+  a.t = t;
+  a.out = out;
+  a.x = x;
+  a.N = N;
+  a.K = int32_t(K);
+  a.batch = batch;
+  a.splits = splits;
+  // Shared memory, from a 1024-aligned base: [weight ring | code2 |
+  // barriers | pair table | x ring (later the partial sums) | block scales].
+  a.off_w = 0;
+  a.off_c2 = uint32_t(kRing * 4096);
+  a.off_bar = a.off_c2 + 1024u;
+  a.off_tab = a.off_bar + 512u;
+  a.off_b = (a.off_tab + 256u * 256u + 1023u) & ~1023u;
+  if (uint32_t(BN * kTileM * 4) > uint32_t(kRing * BN * 128)) return cudaSuccess;  // partial sums fit
+  a.off_scale = a.off_b + uint32_t(kRing * BN * 128);
+  const uint32_t off = a.off_scale + uint32_t(kMaxStagesPerCta * kTileM * 4) + 1024u;  // + slack
+  if (off > 227u * 1024u) return cudaSuccess;
+  // x as a 2-D tensor (K contiguous, `batch` rows) for the tile copies: box
+  // 64 elements (128 bytes, the swizzle span) x BN rows; rows past the batch
+  // read as zero.
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) return cudaSuccess;
+  CUtensorMap tmx;
+  const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(batch)};
+  const cuuint64_t strides[1] = {cuuint64_t(K) * 2u};
+  const cuuint32_t box[2] = {cuuint32_t(kStageK), cuuint32_t(BN)};
+  const cuuint32_t estr[2] = {1u, 1u};
+  if (encode(&tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaSuccess;
+  // packed weights as a 2-D byte tensor (K / 2 bytes per row, N rows): box
+  // 32 bytes x 128 rows; rows past N read as zero
+  CUtensorMap tmw;
+  const cuuint64_t wdims[2] = {cuuint64_t(K / 2), cuuint64_t(N)};
+  const cuuint64_t wstrides[1] = {cuuint64_t(K / 2)};
+  const cuuint32_t wbox[2] = {cuuint32_t(kStageK / 2), cuuint32_t(kTileM)};
+  if (encode(&tmw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(t.packed), wdims, wstrides,
+             wbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaSuccess;
+  *done = true;
+  switch (BN) {
+    case 16: return launch_tc<16>(a, tmx, tmw, grid, off, stream);
+    case 32: return launch_tc<32>(a, tmx, tmw, grid, off, stream);
+    case 48: return launch_tc<48>(a, tmx, tmw, grid, off, stream);
+    default: return launch_tc<64>(a, tmx, tmw, grid, off, stream);
+  }
+}
+
+cudaError_t read_and_clear_tc_flags(unsigned int* flags) {
+  unsigned int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(flags, g_tc_flags, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyToSymbol(g_tc_flags, &zero, sizeof(unsigned int));
+}
+
+}  // namespace nf4

@@ -401,14 +401,22 @@ cudaError_t read_and_clear_device_flags(unsigned int* flags) {
   if (e != cudaSuccess) return e;
   e = read_and_clear_b1_flags(&b1);
   *flags |= b1;
+  if (e != cudaSuccess) return e;
+  e = read_and_clear_tc_flags(&b1);
+  *flags |= b1;
   return e;
 }
 
 cudaError_t launch_gemv(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x, int batch,
                         const YOut& y, cudaStream_t stream) {
   if (batch > 8) {
-    // Wider batches run as slabs of up to eight vectors, one launch each;
-    // after the first slab the weights come from L2.
+    if (K > 0) {
+      bool done = false;
+      const cudaError_t e = try_gemm_tc(t, N, K, x, batch, y, device_sm_count(), stream, &done);
+      if (done || e != cudaSuccess) return e;
+    }
+    // Otherwise slabs of up to eight vectors, one launch each; after the
+    // first slab the weights come from L2.
     const size_t esize = y.dtype == NF4_F32 ? 4 : 2;
     for (int b0 = 0; b0 < batch; b0 += 8) {
       const int nb = batch - b0 < 8 ? batch - b0 : 8;

@@ -226,6 +226,13 @@ cudaError_t try_gemv_b1(const SubTensor* subs, int nsub, int64_t K, const uint16
 // grouped as for batch 1.
 cudaError_t try_gemv_bn(const SubTensor* subs, int nsub, int64_t K, const uint16_t* x, int batch,
                         int sms, cudaStream_t stream, bool* done);
+// Batches 9..64 on the tensor cores (tcgen05.mma with the dequantized weights
+// in tensor memory); *done is false (nothing launched) when the shape or
+// the alignment does not fit (K a multiple of 64, blocksize >= 64 dividing
+// K, 16-byte aligned packed weights and x).
+cudaError_t try_gemm_tc(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x, int batch,
+                        const YOut& out, int sms, cudaStream_t stream, bool* done);
+cudaError_t read_and_clear_tc_flags(unsigned int* flags);
 // Several weights sharing x and K in one launch of the streaming kernels;
 // *done is false (nothing launched) when they cannot share one.
 cudaError_t launch_gemv_group(const QuantTensor* ts, const int64_t* Ns, const YOut* outs, int n,
