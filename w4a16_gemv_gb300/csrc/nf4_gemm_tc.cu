@@ -111,11 +111,14 @@ __device__ __forceinline__ void cluster_sync() {
                    : "memory");
 }
 
-__device__ __forceinline__ float ld_dsmem_f32(uint32_t local_addr, uint32_t rank) {
+__device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t local_addr, uint32_t rank) {
   uint32_t remote;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(remote)
+               : "memory");
   return v;
 }
 
@@ -417,32 +420,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int rows_per = kTileM / p.splits;
   const int rb = split * rows_per;
   const uint32_t red_s = smem_u32(red);
-  const int total = rows_per * p.batch;  // <= 128 * 64 / splits
-  for (int e0 = tid; e0 < total; e0 += 4 * kTcThreads) {
-    float part[4][8];
+  // Four consecutive rows per item (rows_per is a multiple of 16): one
+  // 16-byte load per rank, every rank's load in flight at once.
+  const int quads = rows_per / 4;
+  const int total = quads * p.batch;  // <= 32 * 64 / splits
+  for (int e = tid; e < total; e += kTcThreads) {
+    const int b = e / quads;
+    const int r = rb + 4 * (e - b * quads);
+    float4 part[8];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {  // every load of up to four outputs in flight at once
-      const int e = e0 + u * kTcThreads;
-      const int b = e / rows_per;
-      const int r = rb + (e - b * rows_per);
+    for (int q = 0; q < 8; ++q)
+      part[q] = q < p.splits ? ld_dsmem_f32x4(red_s + uint32_t(b * kTileM + r) * 4u, uint32_t(q))
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 v = part[0];
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        part[u][q] = (e < total && q < p.splits)
-                         ? ld_dsmem_f32(red_s + uint32_t(b * kTileM + r) * 4u, uint32_t(q))
-                         : 0.0f;
-    }
+    for (int q = 1; q < 8; ++q)
+      if (q < p.splits) {  // rank order
+        v.x += part[q].x;
+        v.y += part[q].y;
+        v.z += part[q].z;
+        v.w += part[q].w;
+      }
+    const float vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const int e = e0 + u * kTcThreads;
-      if (e >= total) break;
-      const int b = e / rows_per;
-      const int r = rb + (e - b * rows_per);
-      const int64_t rg = int64_t(tile) * kTileM + r;
-      float v = part[u][0];
-#pragma unroll
-      for (int q = 1; q < 8; ++q)
-        if (q < p.splits) v += part[u][q];  // rank order
-      if (rg < p.N) y_store(p.out, int64_t(b) * p.N + rg, v, y_bias_bits(p.out, rg));
+      const int64_t rg = int64_t(tile) * kTileM + r + u;
+      if (rg < p.N) y_store(p.out, int64_t(b) * p.N + rg, vv[u], y_bias_bits(p.out, rg));
     }
   }
   cluster_sync();  // peers are done reading this CTA's partial sums
