@@ -548,6 +548,31 @@ def decode_step_qwen(dev, gen, code2, batch, layers=28):
     return {"time": time_step, "weight_bytes": wbytes, "launches": 4 * layers, "close": step.close}
 
 
+def run_one_gemv(args):
+    """--gemv N,K,B: --steps launches of one fused GEMV on random codes and
+    scales (a fixed, small command line to put under a profiler)."""
+    import numpy as np
+    import torch
+
+    import w4a16_gemv_gb300 as nf4
+    N, K, B = (int(v) for v in args.gemv.split(","))
+    dev = torch.device("cuda:0")
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(777)
+    code2 = torch.from_numpy((((np.arange(256) - 127.5) / 127.5).astype(np.float16))).to(dev)
+    n = N * K
+    nb = (n + BS - 1) // BS
+    packed = torch.randint(0, 256, (n // 2,), dtype=torch.uint8, device=dev, generator=gen)
+    aq = torch.randint(0, 256, (nb,), dtype=torch.uint8, device=dev, generator=gen)
+    a2 = (torch.rand((nb + S2 - 1) // S2, device=dev, generator=gen) * 0.04 + 0.01).half()
+    x = torch.randn(B, K, device=dev, generator=gen).to(torch.bfloat16)
+    y = torch.empty(B, N, device=dev)
+    for _ in range(args.steps):
+        nf4.nf4_gemv(packed, aq, a2, code2, 0.001, N, K, x, y=y)
+    torch.cuda.synchronize()
+    return {"gemv": [N, K, B], "launches": args.steps, "mean_abs_y": float(y.abs().mean())}
+
+
 def run_decode_step(args):
     """--decode-step: W replays untimed, then K replays back to back between
     two events; one JSON line."""
@@ -752,6 +777,8 @@ def main():
     ap.add_argument("--decode-step", action="store_true",
                     help="time the recorded decode step of a Qwen2.5-1.5B-shaped decoder instead")
     ap.add_argument("--batch", type=int, default=1, help="batch of --decode-step")
+    ap.add_argument("--gemv", type=str, default=None, metavar="N,K,B",
+                    help="run --steps launches of one N x K fused GEMV at batch B (for profilers)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -774,6 +801,10 @@ def main():
     if args.decode_step:
         if rank == 0:
             print(json.dumps(run_decode_step(args)), flush=True)
+        return
+    if args.gemv:
+        if rank == 0:
+            print(json.dumps(run_one_gemv(args)), flush=True)
         return
 
     if world > 1:
