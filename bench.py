@@ -298,6 +298,23 @@ def run_native(args, rank, world, local_rank):
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": roofline, "detail": detail, "gpu_launches": 3 * K, "clocks": clk, "e2e": e2e,
     }
+    if rank == 0 and world == 1 and not args.no_step:
+        # the fused GEMV inside a recorded decode step (after the timed
+        # region): per linear layer, Llama-7B shapes, batch 1
+        del sets
+        torch.cuda.empty_cache()
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(4243)
+        st = decode_step(dev, gen, code2, 1, "llama-7b")
+        us = st["time"](reps=3, m=20)
+        gbs = st["weight_bytes"] / us / 1e3
+        result["decode_step"] = {
+            "model": "llama-7b-shaped (32 layers: q/k/v, o 4096x4096; gate/up 11008x4096; down "
+                     "4096x11008)", "batch": 1, "us_per_step": round(us, 1),
+            "us_per_linear": round(us / st["linears"], 3), "launches_per_step": st["launches"],
+            "weight_bytes": st["weight_bytes"], "gbs": round(gbs, 1),
+            "frac_of_measured_hbm": round(gbs / peak, 4)}
+        st["close"]()
     if rank == 0 and world == 1 and not args.no_cpu:
         result["cpu_baseline"] = cpu_baseline(args, q, x_host, bytes_)
     return result
@@ -492,19 +509,31 @@ def _sweep_time(launch, nsets, reps=5):
     return best
 
 
-def decode_step_qwen(dev, gen, code2, batch, layers=28):
+# Linear layers of one decoder layer: (N, K) of q, k, v, o, gate, up, down.
+DECODERS = {
+    "qwen2.5-1.5b": dict(layers=28, hidden=1536, qkv_bias=True,
+                         shapes=[(1536, 1536), (256, 1536), (256, 1536), (1536, 1536), (8960, 1536),
+                                 (8960, 1536), (1536, 8960)]),
+    "llama-7b": dict(layers=32, hidden=4096, qkv_bias=False,
+                     shapes=[(4096, 4096), (4096, 4096), (4096, 4096), (4096, 4096), (11008, 4096),
+                             (11008, 4096), (4096, 11008)]),
+}
+
+
+def decode_step(dev, gen, code2, batch, model="qwen2.5-1.5b"):
     """A recorded decode step (nf4_step_create) over the linear layers of a
-    Qwen2.5-1.5B-shaped decoder: per layer q/k/v (with bias) from the layer
-    input, o from q, gate/up from o, down from gate; bf16 outputs; random
-    codes and scales (timing does not depend on the values). Returns the
-    step's timer (us per replay, replays back to back on one stream), its
-    weight bytes and its kernel launches per replay (q/k/v and gate/up
-    grouped)."""
+    decoder of the named shape: per layer q/k/v (with bias for Qwen) from the
+    layer input, o from q, gate/up from o, down from gate; bf16 outputs;
+    random codes and scales (timing does not depend on the values). Returns
+    the step's timer (us per replay, replays back to back on one stream), its
+    weight bytes, its linear layers and its kernel launches per replay (q/k/v
+    and gate/up grouped)."""
     import torch
 
     import w4a16_gemv_gb300 as nf4
-    shapes = [(1536, 1536), (256, 1536), (256, 1536), (1536, 1536), (8960, 1536), (8960, 1536),
-              (1536, 8960)]
+    cfg = DECODERS[model]
+    layers = cfg["layers"]
+    shapes = cfg["shapes"]
     inputs = [-1, -1, -1, 0, 3, 3, 4]
     nodes, wbytes = [], 0
     for layer in range(layers):
@@ -520,10 +549,11 @@ def decode_step_qwen(dev, gen, code2, batch, layers=28):
             wbytes += n // 2 + nb + 2 * ng
             inp = inputs[j]
             inp = (-1 if layer == 0 else base - 1) if inp == -1 else base + inp
-            bias = torch.randn(N, device=dev, generator=gen).to(torch.bfloat16) if j < 3 else None
+            bias = (torch.randn(N, device=dev, generator=gen).to(torch.bfloat16)
+                    if j < 3 and cfg["qkv_bias"] else None)
             nodes.append(dict(weight=wt, y=torch.empty((batch, N), dtype=torch.bfloat16, device=dev),
                               bias=bias, input=inp))
-    x = torch.randn((batch, 1536), device=dev, generator=gen).to(torch.bfloat16)
+    x = torch.randn((batch, cfg["hidden"]), device=dev, generator=gen).to(torch.bfloat16)
     step = nf4.DecodeStep(nodes, x)
 
     def time_step(reps=5, m=50):
@@ -545,7 +575,8 @@ def decode_step_qwen(dev, gen, code2, batch, layers=28):
             us = e0.elapsed_time(e1) * 1e3 / m
             best = us if best is None else min(best, us)
         return best
-    return {"time": time_step, "weight_bytes": wbytes, "launches": 4 * layers, "close": step.close}
+    return {"time": time_step, "weight_bytes": wbytes, "launches": 4 * layers, "linears": 7 * layers,
+            "close": step.close}
 
 
 def run_one_gemv(args):
@@ -583,16 +614,19 @@ def run_decode_step(args):
     code2 = torch.from_numpy((((np.arange(256) - 127.5) / 127.5).astype(np.float16))).to(dev)
     gen = torch.Generator(device=dev)
     gen.manual_seed(4242)
-    step = decode_step_qwen(dev, gen, code2, args.batch)
-    us = step["time"](reps=1, m=args.steps) if args.warmup >= 0 else None
+    step = decode_step(dev, gen, code2, args.batch, args.model)
+    us = step["time"](reps=1, m=args.steps)
     gbs = step["weight_bytes"] / us / 1e3
     step["close"]()
-    return {"metric": "decode step us (Qwen2.5-1.5B-shaped, 28 layers x 7 fused GEMVs)",
+    cfg = DECODERS[args.model]
+    return {"metric": f"decode step us ({args.model}-shaped, {cfg['layers']} layers x 7 fused GEMVs)",
             "value": round(us, 1), "unit": "us/step", "higher_is_better": False,
             "batch": args.batch, "steps": args.steps, "launches_per_step": step["launches"],
+            "us_per_linear": round(us / step["linears"], 3),
             "weight_bytes": step["weight_bytes"], "gbs": round(gbs, 1),
             "frac_of_measured_hbm": round(gbs / peak, 4), "peak_kind": peak_kind,
-            "data": "synthetic random codes and scales; weights 676 MB > L2 (no flush needed)"}
+            "data": f"synthetic random codes and scales; weights {step['weight_bytes'] / 1e6:.0f} MB > L2 "
+                    "(no flush needed)"}
 
 
 def run_sweep(args):
@@ -735,16 +769,19 @@ def run_sweep(args):
         del sets
         torch.cuda.empty_cache()
 
-    for batch in (1, 4):
-        step = decode_step_qwen(dev, gen, code2, batch)
-        us, wbytes = step["time"](), step["weight_bytes"]
-        gbs = wbytes / us / 1e3
-        out.append({"kind": "decode_step", "case": "Qwen2.5-1.5B-shaped step, 28 layers x 7 GEMVs",
-                    "batch": batch, "launches": step["launches"], "weight_bytes": wbytes,
-                    "us_per_step": round(us, 1), "gbs": round(gbs, 1),
-                    "frac_of_measured_hbm": round(gbs / peak, 4)})
-        step["close"]()
-        torch.cuda.empty_cache()
+    for model, label in (("qwen2.5-1.5b", "Qwen2.5-1.5B-shaped step, 28 layers x 7 GEMVs"),
+                         ("llama-7b", "Llama-7B-shaped step, 32 layers x 7 GEMVs")):
+        for batch in (1, 4):
+            step = decode_step(dev, gen, code2, batch, model)
+            us, wbytes = step["time"](), step["weight_bytes"]
+            gbs = wbytes / us / 1e3
+            out.append({"kind": "decode_step", "case": label, "batch": batch,
+                        "launches": step["launches"], "weight_bytes": wbytes,
+                        "us_per_step": round(us, 1), "us_per_linear": round(us / step["linears"], 3),
+                        "gbs": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peak, 4)})
+            step["close"]()
+            del step
+            torch.cuda.empty_cache()
 
     for d in out:
         if d["kind"] == "decode_step":
@@ -772,11 +809,14 @@ def main():
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--no-step", action="store_true", help="skip the decode-step detail")
     ap.add_argument("--sweep", action="store_true",
                     help="time every dequant and GEMV configuration instead of the step")
     ap.add_argument("--decode-step", action="store_true",
                     help="time the recorded decode step of a Qwen2.5-1.5B-shaped decoder instead")
     ap.add_argument("--batch", type=int, default=1, help="batch of --decode-step")
+    ap.add_argument("--model", choices=sorted(DECODERS), default="qwen2.5-1.5b",
+                    help="decoder shape of --decode-step")
     ap.add_argument("--gemv", type=str, default=None, metavar="N,K,B",
                     help="run --steps launches of one N x K fused GEMV at batch B (for profilers)")
     args = ap.parse_args()
