@@ -87,10 +87,11 @@ NF4_API int nf4_last_cuda_error(void);
 
 /*
  * nf4_device_error_flags -- read and clear the library's device-side error
- * flags. Bit 0 is set when a kernel's bounded wait for its own asynchronous
- * global->shared copies ran out (about one second); that kernel then writes
- * NaN to the outputs it owns and returns instead of hanging. Synchronises
- * with the device (cudaMemcpyFromSymbol). `flags` is a host pointer.
+ * flags. Bit 0 is set when a bounded wait of the tensor-core GEMV (batches
+ * 9..64) on its own copy or MMA pipeline ran out (about one second); that
+ * launch then writes NaN or incomplete values to its outputs and finishes
+ * instead of hanging. Synchronises with the device (cudaMemcpyFromSymbol).
+ * `flags` is a host pointer.
  * Errors: NF4_ERR_NULL, NF4_ERR_CUDA.
  */
 NF4_API nf4_status nf4_device_error_flags(unsigned int* flags);

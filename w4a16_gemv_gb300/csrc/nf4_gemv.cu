@@ -33,23 +33,6 @@ constexpr int kWarps = kThreads / 32;
 
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 
-// 32-bit shared-window loads.
-__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ uint4 lds_u128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ uint2 lds_u64(uint32_t addr) {
-  uint2 v;
-  asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
-  return v;
-}
-
 // Two bfloat16 (low half = lower-index element) widened to binary32 (exact).
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
   return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
@@ -258,8 +241,6 @@ __global__ void __launch_bounds__(kThreads) gemv_generic_kernel(QuantTensor t, i
   }
 }
 
-__device__ unsigned int g_device_flags = 0;
-
 // ---- row-streaming kernel (batch > 1) and generic kernel launchers -----------
 
 constexpr size_t kTableBytes = 256 * 32 * sizeof(uint32_t);
@@ -394,17 +375,8 @@ cudaError_t dispatch_batch(const QuantTensor& t, int64_t N, int64_t K, const uin
 }  // namespace
 
 cudaError_t read_and_clear_device_flags(unsigned int* flags) {
-  unsigned int zero = 0, b1 = 0;
-  cudaError_t e = cudaMemcpyFromSymbol(flags, g_device_flags, sizeof(unsigned int));
-  if (e != cudaSuccess) return e;
-  e = cudaMemcpyToSymbol(g_device_flags, &zero, sizeof(unsigned int));
-  if (e != cudaSuccess) return e;
-  e = read_and_clear_b1_flags(&b1);
-  *flags |= b1;
-  if (e != cudaSuccess) return e;
-  e = read_and_clear_tc_flags(&b1);
-  *flags |= b1;
-  return e;
+  // the tensor-core GEMV is the only kernel with waits that can run out
+  return read_and_clear_tc_flags(flags);
 }
 
 cudaError_t launch_gemv(const QuantTensor& t, int64_t N, int64_t K, const uint16_t* x, int batch,

@@ -1135,9 +1135,5 @@ cudaError_t try_gemv_bn(const SubTensor* subs, int nsub, int64_t K, const uint16
   return launch_bn_n<8, 4>(a, grid, smem, stream);
 }
 
-cudaError_t read_and_clear_b1_flags(unsigned int* flags) {
-  *flags = 0u;  // the batch-1 kernel has no waits that can run out
-  return cudaSuccess;
-}
 
 }  // namespace nf4

@@ -131,8 +131,7 @@ cudaError_t quantize_static_scratch(void** ptr);
 namespace nf4 {
 
 // ---------------------------------------------------------------------------
-// Bulk asynchronous copies (cp.async.bulk) completing on shared-memory
-// mbarriers, for sm_90+ (used on sm_103a).
+// Shared-memory mbarriers (the tensor-core GEMV's copy and MMA pipeline).
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -147,31 +146,10 @@ __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
                "r"(bytes)
                : "memory");
-}
-
-// Global -> shared bulk copy of `bytes` (multiple of 16, both addresses
-// 16-byte aligned); completion is signalled on `bar` as transaction bytes.
-__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
-                                              uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// Bulk prefetch of global memory into L2 (size a multiple of 16, address
-// 16-byte aligned).
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
@@ -205,7 +183,6 @@ constexpr long long kWaitLimitCycles = 2000000000ll;
 // Device-side error flags (bit 0: a bounded wait timed out). Read and cleared
 // by nf4_device_error_flags().
 cudaError_t read_and_clear_device_flags(unsigned int* flags);
-cudaError_t read_and_clear_b1_flags(unsigned int* flags);
 
 // One weight of a GEMV launch that may serve several weights sharing x.
 struct SubTensor {
