@@ -45,7 +45,7 @@ constexpr int kTileM = 128;
 constexpr int kStageK = 64;      // elements of K per stage
 constexpr int kRing = 8;         // stages of packed weights and x in shared memory
 constexpr int kAhead = kRing - 2;  // stages loaded ahead of the one being dequantized
-constexpr int kMaxStagesPerCta = 64;
+constexpr int kLongStages = 64;  // stages per CTA above which K is split further
 constexpr int kNA = 4;               // A buffers in TMEM (the producers' lead over the MMAs)
 constexpr uint32_t kTmemCols = 512;  // A: kNA buffers x 64 columns (hi 32 + lo 32); D: 256..319
 
@@ -59,7 +59,7 @@ struct TcArgs {
   int32_t K;
   int batch;
   int splits;  // CTAs per cluster, along K (1, 2, 4 or 8)
-  uint32_t off_b, off_w, off_scale, off_tab, off_c2, off_bar;
+  uint32_t off_b, off_w, off_recv, off_tab, off_c2, off_bar;
 };
 
 
@@ -109,17 +109,6 @@ __device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t (&v)[4]) {
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                    : "memory");
-}
-
-__device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t local_addr, uint32_t rank) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(remote)
-               : "memory");
-  return v;
 }
 
 // Packed binary32 multiply and subtract (two independent IEEE operations,
@@ -201,7 +190,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t sbase = smem_u32(smem);
   const uint32_t b_ring = sbase + p.off_b;                    // kRing slots of BN x 128 B
   const uint32_t w_ring = sbase + p.off_w;                    // kRing slots of 4 KB
-  float* sScale = reinterpret_cast<float*>(smem + p.off_scale);  // [stage][128]
+  float* recv = reinterpret_cast<float*>(smem + p.off_recv);  // [src rank][BN][128 / splits]
   float* sC2 = reinterpret_cast<float*>(smem + p.off_c2);
   uint64_t* afull = reinterpret_cast<uint64_t*>(smem + p.off_bar);  // A buffer written (16 warps)
   uint64_t* aempty = afull + kNA;  // MMAs of the A buffer done
@@ -209,7 +198,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* xempty = xfull + kRing;  // MMAs reading the x slot done
   uint64_t* wfull = xempty + kRing;  // weight tile landed, per slot
   uint32_t* s_taddr = reinterpret_cast<uint32_t*>(smem + p.off_bar + 8 * (2 * kNA + 3 * kRing));
-  float* red = reinterpret_cast<float*>(smem + p.off_b);     // [BN][128] after the main loop
 
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -233,22 +221,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   const bool producer = warp < kProducerWarps;
   // Small inputs first (their latency hides behind the table build): the
-  // code2 entry of this thread, and the absmax_q / absmax2 of this row for
-  // its first stages (stages i = kq mod 4; the rest below if more than 32).
+  // code2 entry of this thread, and the block-scale inputs (absmax_q,
+  // absmax2) of this row for the first three stages; the producers keep
+  // them in a three-stage shift chain, loading each stage's three ahead.
   const uint16_t c2v = tid < 256 ? __ldg(t.code2 + tid) : uint16_t(0);
-  uint8_t q0[8];
-  uint16_t a20[8];
-#pragma unroll
-  for (int u = 0; u < 8; ++u) {
-    const int i = kq + 4 * u;
-    q0[u] = 0;
-    a20[u] = 0;
+  auto load_scale_in = [&](int i, uint32_t& q, uint32_t& a2) {
+    q = 0u;
+    a2 = 0u;
     if (producer && i < ns && row_ok) {
       const int64_t blk = (r_glob * K + int64_t(s0 + i) * kStageK) >> t.lbs;
-      q0[u] = __ldg(t.absmax_q + blk);
-      a20[u] = __ldg(t.absmax2 + (blk >> t.ls2));
+      q = __ldg(t.absmax_q + blk);
+      a2 = __ldg(t.absmax2 + (blk >> t.ls2));
     }
-  }
+  };
+  uint32_t q_0, q_1, q_2, a_0, a_1, a_2;
+  load_scale_in(0, q_0, a_0);
+  load_scale_in(1, q_1, a_1);
+  load_scale_in(2, q_2, a_2);
   // The weight and x tiles of stage i into ring slot i % kRing (thread
   // kTcThreads - 32 only).
   auto issue_tiles = [&](int i) {
@@ -260,6 +249,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tma_load_2d(b_ring + uint32_t(slot) * uint32_t(BN * 128), &tmx, (s0 + i) * kStageK, 0, &xfull[slot]);
   };
   __syncthreads();  // barriers initialised before any copy uses one
+  // First phase of the cluster barrier: this CTA is running (its shared
+  // memory may receive the peers' partial sums once the phase completes).
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   if (warp == kCopyWarp && lane == 0)
     for (int i = 0; i < kAhead && i < ns; ++i) issue_tiles(i);
 
@@ -278,30 +270,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (tid < 256) sC2[tid] = half_bits_to_float(c2v);
   __syncthreads();  // sC2 ready
 
-  // Block scales of this thread's row for the CTA's stages (stages i = kq
-  // mod 4): fp32(fp32(code2[q] * absmax2[g]) + offset); 0 past the last row.
-  for (int i0 = kq; producer && i0 < ns; i0 += 32) {
-    uint8_t q[8];
-    uint16_t a2[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int i = i0 + 4 * u;
-      q[u] = q0[u];
-      a2[u] = a20[u];
-      if (i0 != kq && i < ns && row_ok) {
-        const int64_t blk = (r_glob * K + int64_t(s0 + i) * kStageK) >> t.lbs;
-        q[u] = __ldg(t.absmax_q + blk);
-        a2[u] = __ldg(t.absmax2 + (blk >> t.ls2));
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int i = i0 + 4 * u;
-      if (i < ns)
-        sScale[i * kTileM + row] =
-            row_ok ? __fadd_rn(__fmul_rn(sC2[q[u]], half_bits_to_float(a2[u])), t.offset) : 0.0f;
-    }
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -324,7 +292,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
       // dequantize 16 elements (8 packed bytes) of this row: w_hat = fp32(NF4
       // code * s), split into bfloat16 hi + lo (scale 0 past the last row)
-      const float sc = sScale[i * kTileM + row];
+      // block scale fp32(fp32(code2[q] * absmax2[g]) + offset); 0 past the last row
+      const float sc =
+          row_ok ? __fadd_rn(__fmul_rn(sC2[q_0], half_bits_to_float(uint16_t(a_0))), t.offset) : 0.0f;
+      q_0 = q_1;
+      a_0 = a_1;
+      q_1 = q_2;
+      a_1 = a_2;
+      load_scale_in(i + 3, q_2, a_2);
       const float2 sc2 = make_float2(sc, sc);
       uint32_t wd0, wd1;
       asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];"
@@ -399,56 +374,47 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (ns > 0)
     ok = mbar_wait_bounded(&aempty[(ns - 1) % kNA], uint32_t(((ns - 1) / kNA) & 1), kWaitLimitCycles) && ok;
   tc_fence_after();
-  __syncthreads();  // the x ring is free: it becomes the partial-sum buffer
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // every peer is running
 
-  // This CTA's partial sums D[row][n] -> red[n][row]; warp (row quarter,
-  // K quarter kq) copies columns [kq * BN / 4, (kq + 1) * BN / 4).
-#pragma unroll
-  for (int c0 = 0; c0 < BN / 4 && producer; c0 += 4) {
-    uint32_t v[4];
-    tmem_ld4(lane_base + 64u * kNA + uint32_t(kq * (BN / 4) + c0), v);
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      red[(kq * (BN / 4) + c0 + j) * kTileM + row] = ok ? __uint_as_float(v[j]) : __uint_as_float(0x7fc00000u);
-  }
-  if (!ok) atomicOr(&g_tc_flags, 1u);
-  cluster_sync();  // every rank's partial sums are written
-
-  // Rows [split * 128 / splits, (split + 1) * 128 / splits) of the tile:
-  // the sum over ranks in rank order, then the output stage.
+  // Split-K: the CTA owning rows [rank * R, (rank + 1) * R) of the tile (R
+  // = 128 / splits) receives every rank's partial sums of those rows in its
+  // own receive buffer (not used before, so peers may write as soon as their
+  // MMAs are done); warp (row quarter, K quarter kq) pushes columns
+  // [kq * BN / 4, (kq + 1) * BN / 4) of its lanes' rows.
   const int rows_per = kTileM / p.splits;
-  const int rb = split * rows_per;
-  const uint32_t red_s = smem_u32(red);
-  // Four consecutive rows per item (rows_per is a multiple of 16): one
-  // 16-byte load per rank, every rank's load in flight at once.
-  const int quads = rows_per / 4;
-  const int total = quads * p.batch;  // <= 32 * 64 / splits
-  for (int e = tid; e < total; e += kTcThreads) {
-    const int b = e / quads;
-    const int r = rb + 4 * (e - b * quads);
-    float4 part[8];
+  {
+    const int owner = row / rows_per;
+    const int rl = row - owner * rows_per;
+    uint32_t dst = smem_u32(recv) + uint32_t((split * BN) * rows_per + rl) * 4u;
+    asm volatile("mapa.shared::cluster.u32 %0, %0, %1;" : "+r"(dst) : "r"(uint32_t(owner)));
 #pragma unroll
-    for (int q = 0; q < 8; ++q)
-      part[q] = q < p.splits ? ld_dsmem_f32x4(red_s + uint32_t(b * kTileM + r) * 4u, uint32_t(q))
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
-    float4 v = part[0];
+    for (int c0 = 0; c0 < BN / 4 && producer; c0 += 4) {
+      uint32_t v[4];
+      tmem_ld4(lane_base + 64u * kNA + uint32_t(kq * (BN / 4) + c0), v);
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-    for (int q = 1; q < 8; ++q)
-      if (q < p.splits) {  // rank order
-        v.x += part[q].x;
-        v.y += part[q].y;
-        v.z += part[q].z;
-        v.w += part[q].w;
+      for (int j = 0; j < 4; ++j) {
+        const int n = kq * (BN / 4) + c0 + j;
+        const float f = ok ? __uint_as_float(v[j]) : __uint_as_float(0x7fc00000u);
+        asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dst + uint32_t(n * rows_per) * 4u), "f"(f)
+                     : "memory");
       }
-    const float vv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int64_t rg = int64_t(tile) * kTileM + r + u;
-      if (rg < p.N) y_store(p.out, int64_t(b) * p.N + rg, vv[u], y_bias_bits(p.out, rg));
     }
   }
-  cluster_sync();  // peers are done reading this CTA's partial sums
+  if (!ok) atomicOr(&g_tc_flags, 1u);
+  cluster_sync();  // every rank's pushes have landed
+
+  // Rows [split * R, (split + 1) * R): the sum over ranks in rank order,
+  // then the output stage.
+  const int total = rows_per * p.batch;
+  for (int e = tid; e < total; e += kTcThreads) {
+    const int b = e / rows_per;
+    const int rl = e - b * rows_per;
+    const int64_t rg = int64_t(tile) * kTileM + split * rows_per + rl;
+    float v = recv[(0 * BN + b) * rows_per + rl];
+    for (int q = 1; q < p.splits; ++q) v += recv[(q * BN + b) * rows_per + rl];
+    if (rg < p.N) y_store(p.out, int64_t(b) * p.N + rg, v, y_bias_bits(p.out, rg));
+  }
 
   tc_fence_before();
   __syncthreads();
@@ -516,12 +482,11 @@ cudaError_t try_gemm_tc(const QuantTensor& t, int64_t N, int64_t K, const uint16
   const int64_t tiles = (N + kTileM - 1) / kTileM;
   const int S = int(K / kStageK);
   if (tiles > (int64_t(1) << 24)) return cudaSuccess;
-  // K split over a cluster: fill the SMs, at most 64 stages (4096 elements)
-  // and at least 4 stages per CTA.
+  // K split over a cluster of up to 8: fill the SMs, keep at least 4 stages
+  // per CTA, and split long rows (more than 64 stages, 4096 elements).
   int splits = 1;
-  while (splits < 8 && (S + splits - 1) / splits > kMaxStagesPerCta) splits *= 2;
+  while (splits < 8 && (S + splits - 1) / splits > kLongStages) splits *= 2;
   while (splits < 8 && tiles * splits * 2 <= sms && S / (splits * 2) >= 4) splits *= 2;
-  if ((S + splits - 1) / splits > kMaxStagesPerCta) return cudaSuccess;
   const int grid = int(tiles) * splits;
 
   TcArgs a;
@@ -533,15 +498,14 @@ cudaError_t try_gemm_tc(const QuantTensor& t, int64_t N, int64_t K, const uint16
   a.batch = batch;
   a.splits = splits;
   // Shared memory, from a 1024-aligned base: [weight ring | code2 |
-  // barriers | pair table | x ring (later the partial sums) | block scales].
+  // barriers | pair table | x ring | split-K receive buffer].
   a.off_w = 0;
   a.off_c2 = uint32_t(kRing * 4096);
   a.off_bar = a.off_c2 + 1024u;
   a.off_tab = a.off_bar + 512u;
   a.off_b = (a.off_tab + 256u * 256u + 1023u) & ~1023u;
-  if (uint32_t(BN * kTileM * 4) > uint32_t(kRing * BN * 128)) return cudaSuccess;  // partial sums fit
-  a.off_scale = a.off_b + uint32_t(kRing * BN * 128);
-  const uint32_t off = a.off_scale + uint32_t(kMaxStagesPerCta * kTileM * 4) + 1024u;  // + slack
+  a.off_recv = a.off_b + uint32_t(kRing * BN * 128);  // receive buffer of the split-K sums
+  const uint32_t off = a.off_recv + uint32_t(BN * kTileM * 4) + 1024u;  // + slack
   if (off > 227u * 1024u) return cudaSuccess;
   // x as a 2-D tensor (K contiguous, `batch` rows) for the tile copies: box
   // 64 elements (128 bytes, the swizzle span) x BN rows; rows past the batch
