@@ -18,7 +18,7 @@
 //     swizzled, K-major;
 //   * one warp issues tcgen05.mma (kind::f16, bf16 x bf16 -> fp32 in TMEM),
 //     two per 16-element K step (hi and lo), once the producer warps have
-//     signalled the stage's A buffer full; its commits free the A buffer and
+//     signalled the stage's A buffer full; its commit frees the A buffer and
 //     the ring slot, which another warp refills with the tile copies. The producers run
 //     up to four stages ahead of the MMAs (four A buffers in TMEM);
 //   * K is split over a thread-block cluster; partial sums are added in rank
@@ -179,11 +179,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int row = (warp & 3) * 32 + lane;   // row of the tile = TMEM lane
   const int tile = int(blockIdx.x) / p.splits;
   const int split = int(blockIdx.x) - tile * p.splits;  // rank in the cluster
-  const int64_t r_glob = int64_t(tile) * kTileM + row;
-  const bool row_ok = r_glob < p.N;
   const QuantTensor& t = p.t;
   const int64_t K = p.K;
   const int S = int(K / kStageK);
+  const int64_t r_glob = int64_t(tile) * kTileM + row;
+  const bool row_ok = r_glob < p.N;
   const int s0 = int(int64_t(split) * S / p.splits);
   const int ns = int(int64_t(split + 1) * S / p.splits) - s0;
 
@@ -193,11 +193,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   float* recv = reinterpret_cast<float*>(smem + p.off_recv);  // [src rank][BN][128 / splits]
   float* sC2 = reinterpret_cast<float*>(smem + p.off_c2);
   uint64_t* afull = reinterpret_cast<uint64_t*>(smem + p.off_bar);  // A buffer written (16 warps)
-  uint64_t* aempty = afull + kNA;  // MMAs of the A buffer done
-  uint64_t* xfull = afull + 2 * kNA;  // x tile landed, per slot
-  uint64_t* xempty = xfull + kRing;  // MMAs reading the x slot done
-  uint64_t* wfull = xempty + kRing;  // weight tile landed, per slot
-  uint32_t* s_taddr = reinterpret_cast<uint32_t*>(smem + p.off_bar + 8 * (2 * kNA + 3 * kRing));
+  uint64_t* mdone = afull + kNA;  // MMAs of a stage done (frees its A buffer and ring slot), per slot
+  uint64_t* full = mdone + kRing;  // weight and x tiles landed, per slot
+  uint32_t* s_taddr = reinterpret_cast<uint32_t*>(smem + p.off_bar + 8 * (kNA + 2 * kRing));
 
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -207,23 +205,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   if (tid == 0) {
-    for (int i = 0; i < kNA; ++i) {
-      mbar_init(&afull[i], kProducerWarps);
-      mbar_init(&aempty[i], 1);
-    }
+    for (int i = 0; i < kNA; ++i) mbar_init(&afull[i], kProducerWarps);
     for (int i = 0; i < kRing; ++i) {
-      mbar_init(&xfull[i], 1);
-      mbar_init(&xempty[i], 1);
-      mbar_init(&wfull[i], 1);
+      mbar_init(&mdone[i], 1);
+      mbar_init(&full[i], 1);
     }
     fence_mbar_init();
   }
 
+  // Waits until the MMAs of stage j (and every earlier stage) are done: the
+  // commit of stage j arrives on mdone[j % kRing]; a barrier is reused only
+  // after every waiter of its previous phase has passed.
+  auto wait_mma_done = [&](int j) {
+    return mbar_wait_bounded(&mdone[j % kRing], uint32_t((j / kRing) & 1), kWaitLimitCycles);
+  };
   const bool producer = warp < kProducerWarps;
   // Small inputs first (their latency hides behind the table build): the
   // code2 entry of this thread, and the block-scale inputs (absmax_q,
-  // absmax2) of this row for the first three stages; the producers keep
-  // them in a three-stage shift chain, loading each stage's three ahead.
+  // absmax2) of this row for the first kNA stages; a producer loads those of
+  // stages kNA .. kRing - 1 during its first kNA stages, and those of stage
+  // i + kRing at stage i, into the registers stage i used (the loop is
+  // unrolled over the ring, so no register is copied while its load is in
+  // flight).
   const uint16_t c2v = tid < 256 ? __ldg(t.code2 + tid) : uint16_t(0);
   auto load_scale_in = [&](int i, uint32_t& q, uint32_t& a2) {
     q = 0u;
@@ -234,20 +237,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       a2 = __ldg(t.absmax2 + (blk >> t.ls2));
     }
   };
-  uint32_t q_0, q_1, q_2, a_0, a_1, a_2;
-  load_scale_in(0, q_0, a_0);
-  load_scale_in(1, q_1, a_1);
-  load_scale_in(2, q_2, a_2);
+  uint32_t qv[kRing], av[kRing];
+#pragma unroll
+  for (int u = 0; u < kNA; ++u) load_scale_in(u, qv[u], av[u]);
   // The weight and x tiles of stage i into ring slot i % kRing (thread
   // kTcThreads - 32 only).
   auto issue_tiles = [&](int i) {
     const int slot = i % kRing;
-    mbar_arrive_expect_tx(&wfull[slot], uint32_t(kTileM * kStageK / 2));
+    mbar_arrive_expect_tx(&full[slot], uint32_t(kTileM * kStageK / 2 + BN * 128));
     tma_load_2d(w_ring + uint32_t(slot) * 4096u, &tmw, (s0 + i) * (kStageK / 2), tile * kTileM,
-                &wfull[slot]);
-    mbar_arrive_expect_tx(&xfull[slot], uint32_t(BN * 128));
-    tma_load_2d(b_ring + uint32_t(slot) * uint32_t(BN * 128), &tmx, (s0 + i) * kStageK, 0, &xfull[slot]);
+                &full[slot]);
+    tma_load_2d(b_ring + uint32_t(slot) * uint32_t(BN * 128), &tmx, (s0 + i) * kStageK, 0, &full[slot]);
   };
+
   __syncthreads();  // barriers initialised before any copy uses one
   // First phase of the cluster barrier: this CTA is running (its shared
   // memory may receive the peers' partial sums once the phase completes).
@@ -282,47 +284,53 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (producer) {
 #pragma unroll 1
-    for (int i = 0; i < ns; ++i) {
-      const int buf = i % kNA;
-      if (i >= kNA) {  // the MMAs of stage i - kNA have read A buffer `buf`
-        ok = mbar_wait_bounded(&aempty[buf], uint32_t(((i - kNA) / kNA) & 1), kWaitLimitCycles) && ok;
-        tc_fence_after();
-      }
-      ok = mbar_wait_bounded(&wfull[i % kRing], uint32_t((i / kRing) & 1), kWaitLimitCycles) && ok;
-
-      // dequantize 16 elements (8 packed bytes) of this row: w_hat = fp32(NF4
-      // code * s), split into bfloat16 hi + lo (scale 0 past the last row)
-      // block scale fp32(fp32(code2[q] * absmax2[g]) + offset); 0 past the last row
-      const float sc =
-          row_ok ? __fadd_rn(__fmul_rn(sC2[q_0], half_bits_to_float(uint16_t(a_0))), t.offset) : 0.0f;
-      q_0 = q_1;
-      a_0 = a_1;
-      q_1 = q_2;
-      a_1 = a_2;
-      load_scale_in(i + 3, q_2, a_2);
-      const float2 sc2 = make_float2(sc, sc);
-      uint32_t wd0, wd1;
-      asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];"
-                   : "=r"(wd0), "=r"(wd1)
-                   : "r"(w_ring + uint32_t(i % kRing) * 4096u + uint32_t(row) * 32u + uint32_t(kq) * 8u));
-      uint32_t hi[8], lo[8];
+    for (int i0 = 0; i0 < ns; i0 += kRing) {
+      const uint32_t ph = uint32_t(i0 / kRing) & 1u;  // ring phase of stages i0 .. i0 + kRing - 1
 #pragma unroll
-      for (int b = 0; b < 8; ++b) {
-        const uint32_t word = b < 4 ? wd0 : wd1;
-        const uint32_t addr = tab_lane + (__byte_perm(word, 0u, 0x4440u + uint32_t(b & 3)) << 8);
-        float2 c;
-        asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(c.x), "=f"(c.y) : "r"(addr));
-        const float2 w = fmul2_rn(c, sc2);
-        hi[b] = bf16x2_rn(w);
-        lo[b] = bf16x2_rn(fsub2_rn(w, bf16x2_to_f2(hi[b])));  // exact residual
+      for (int u = 0; u < kRing; ++u) {  // stage i0 + u: ring slot u, A buffer u % kNA
+        const int i = i0 + u;
+        if (i < ns) {
+          if (i >= kNA) {  // the MMAs of stage i - kNA (slot (u - kNA) mod kRing) have read A buffer u % kNA
+            const uint32_t ph_prev = u >= kNA ? ph : ph ^ 1u;
+            ok = mbar_wait_bounded(&mdone[(u + kRing - kNA) % kRing], ph_prev, kWaitLimitCycles) && ok;
+            tc_fence_after();
+          }
+          // both tiles of the stage landed (the MMAs of the stage read the x
+          // tile after this wait, through the A-buffer barrier)
+          ok = mbar_wait_bounded(&full[u], ph, kWaitLimitCycles) && ok;
+
+          // block scale fp32(fp32(code2[q] * absmax2[g]) + offset); 0 past the last row
+          const float sc =
+              row_ok ? __fadd_rn(__fmul_rn(sC2[qv[u]], half_bits_to_float(uint16_t(av[u]))), t.offset) : 0.0f;
+          load_scale_in(i + kRing, qv[u], av[u]);
+          if (u < kRing - kNA && i0 == 0) load_scale_in(u + kNA, qv[u + kNA], av[u + kNA]);
+          const float2 sc2 = make_float2(sc, sc);
+          // dequantize 16 elements (8 packed bytes) of this row: w_hat = fp32(NF4
+          // code * s), split into bfloat16 hi + lo
+          uint32_t wd0, wd1;
+          asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];"
+                       : "=r"(wd0), "=r"(wd1)
+                       : "r"(w_ring + uint32_t(u) * 4096u + uint32_t(row) * 32u + uint32_t(kq) * 8u));
+          uint32_t hi[8], lo[8];
+#pragma unroll
+          for (int b = 0; b < 8; ++b) {
+            const uint32_t word = b < 4 ? wd0 : wd1;
+            const uint32_t addr = tab_lane + (__byte_perm(word, 0u, 0x4440u + uint32_t(b & 3)) << 8);
+            float2 c;
+            asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(c.x), "=f"(c.y) : "r"(addr));
+            const float2 w = fmul2_rn(c, sc2);
+            hi[b] = bf16x2_rn(w);
+            lo[b] = bf16x2_rn(fsub2_rn(w, bf16x2_to_f2(hi[b])));  // exact residual
+          }
+          const uint32_t acol = lane_base + uint32_t(u % kNA) * 64u + uint32_t(kq) * 8u;
+          tmem_st8(acol, hi);
+          tmem_st8(acol + 32u, lo);
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&afull[u % kNA]);
+        }
       }
-      const uint32_t acol = lane_base + uint32_t(buf) * 64u + uint32_t(kq) * 8u;
-      tmem_st8(acol, hi);
-      tmem_st8(acol + 32u, lo);
-      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&afull[buf]);
     }
   } else if (warp == kMmaWarp && lane == 0) {
     // MMA issue. One thread, sharing its scheduler with producer warps: the
@@ -332,30 +340,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // field).
     const uint64_t desc0 = desc_sw128(b_ring);
     constexpr uint32_t kSlotUnits = uint32_t(BN * 128) >> 4;
-    uint32_t slot = 0, slot_ph = 0, abuf = 0, a_ph = 0;
+    static_assert(kRing % kNA == 0, "ring slots and A buffers advance together");
 #pragma unroll 1
-    for (int i = 0; i < ns; ++i) {
-      ok = mbar_wait_bounded(&afull[abuf], a_ph, kWaitLimitCycles) && ok;
-      ok = mbar_wait_bounded(&xfull[slot], slot_ph, kWaitLimitCycles) && ok;
-      tc_fence_after();
-      const uint32_t a_t = tbase + abuf * 64u;
-      const uint64_t bd = desc0 + uint64_t(slot * kSlotUnits);
-      mma_bf16(d_col, a_t, bd, kIdesc, i > 0 ? 1u : 0u);
-      mma_bf16(d_col, a_t + 32u, bd, kIdesc, 1u);
+    for (int i0 = 0; i0 < ns; i0 += kRing) {
+      const uint32_t a_ph0 = uint32_t(i0 / kNA) & 1u;
 #pragma unroll
-      for (int j = 1; j < kStageK / 16; ++j) {  // 32 bytes of K per step
-        mma_bf16(d_col, a_t + 8u * uint32_t(j), bd + uint64_t(2 * j), kIdesc, 1u);
-        mma_bf16(d_col, a_t + 32u + 8u * uint32_t(j), bd + uint64_t(2 * j), kIdesc, 1u);
-      }
-      tc_commit(&aempty[abuf]);
-      tc_commit(&xempty[slot]);
-      if (++abuf == uint32_t(kNA)) {
-        abuf = 0;
-        a_ph ^= 1u;
-      }
-      if (++slot == uint32_t(kRing)) {
-        slot = 0;
-        slot_ph ^= 1u;
+      for (int u = 0; u < kRing; ++u) {  // stage i0 + u: slot u, A buffer u % kNA
+        if (i0 + u < ns) {
+          ok = mbar_wait_bounded(&afull[u % kNA], a_ph0 ^ uint32_t((u / kNA) & 1), kWaitLimitCycles) && ok;
+          tc_fence_after();
+          const uint32_t a_t = tbase + uint32_t(u % kNA) * 64u;
+          const uint64_t bd = desc0 + uint64_t(u * kSlotUnits);
+          mma_bf16(d_col, a_t, bd, kIdesc, (i0 + u) > 0 ? 1u : 0u);
+          mma_bf16(d_col, a_t + 32u, bd, kIdesc, 1u);
+#pragma unroll
+          for (int j = 1; j < kStageK / 16; ++j) {  // 32 bytes of K per step
+            mma_bf16(d_col, a_t + 8u * uint32_t(j), bd + uint64_t(2 * j), kIdesc, 1u);
+            mma_bf16(d_col, a_t + 32u + 8u * uint32_t(j), bd + uint64_t(2 * j), kIdesc, 1u);
+          }
+          tc_commit(&mdone[u]);  // frees A buffer u % kNA and ring slot u
+        }
       }
     }
   } else if (warp == kCopyWarp && lane == 0) {
@@ -365,14 +369,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll 1
     for (int nx = kAhead; nx < ns; ++nx) {
       if (nx >= kRing)
-        ok = mbar_wait_bounded(&xempty[nx & (kRing - 1)], uint32_t(((nx >> 3) + 1) & 1), kWaitLimitCycles) && ok;
+        ok = wait_mma_done(nx - kRing) && ok;
       issue_tiles(nx);
     }
   }
   __syncwarp();
   // all MMAs done (the last commit covers every earlier one)
   if (ns > 0)
-    ok = mbar_wait_bounded(&aempty[(ns - 1) % kNA], uint32_t(((ns - 1) / kNA) & 1), kWaitLimitCycles) && ok;
+    ok = wait_mma_done(ns - 1) && ok;
   tc_fence_after();
   asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // every peer is running
 
@@ -387,14 +391,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int rl = row - owner * rows_per;
     uint32_t dst = smem_u32(recv) + uint32_t((split * BN) * rows_per + rl) * 4u;
     asm volatile("mapa.shared::cluster.u32 %0, %0, %1;" : "+r"(dst) : "r"(uint32_t(owner)));
+    if (producer) {
+      // all BN / 4 columns of this warp's quarter, then one wait
+      uint32_t v[BN / 4];
 #pragma unroll
-    for (int c0 = 0; c0 < BN / 4 && producer; c0 += 4) {
-      uint32_t v[4];
-      tmem_ld4(lane_base + 64u * kNA + uint32_t(kq * (BN / 4) + c0), v);
+      for (int c0 = 0; c0 < BN / 4; c0 += 4) {
+        uint32_t w4[4];
+        tmem_ld4(lane_base + 64u * kNA + uint32_t(kq * (BN / 4) + c0), w4);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[c0 + j] = w4[j];
+      }
       asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int n = kq * (BN / 4) + c0 + j;
+      for (int j = 0; j < BN / 4; ++j) asm volatile("" : "+r"(v[j]));  // uses follow the wait
+#pragma unroll
+      for (int j = 0; j < BN / 4; ++j) {
+        const int n = kq * (BN / 4) + j;
         const float f = ok ? __uint_as_float(v[j]) : __uint_as_float(0x7fc00000u);
         asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dst + uint32_t(n * rows_per) * 4u), "f"(f)
                      : "memory");
@@ -406,13 +418,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   // Rows [split * R, (split + 1) * R): the sum over ranks in rank order,
   // then the output stage.
+  const int lrp = 31 - __clz(rows_per);  // rows_per is a power of two
   const int total = rows_per * p.batch;
+  const int64_t rg0 = int64_t(tile) * kTileM + split * rows_per;
   for (int e = tid; e < total; e += kTcThreads) {
-    const int b = e / rows_per;
-    const int rl = e - b * rows_per;
-    const int64_t rg = int64_t(tile) * kTileM + split * rows_per + rl;
-    float v = recv[(0 * BN + b) * rows_per + rl];
-    for (int q = 1; q < p.splits; ++q) v += recv[(q * BN + b) * rows_per + rl];
+    const int b = e >> lrp;
+    const int rl = e & (rows_per - 1);
+    const int64_t rg = rg0 + rl;
+    const float* src = recv + b * rows_per + rl;
+    float v = src[0];
+#pragma unroll
+    for (int q = 1; q < 8; ++q)
+      if (q < p.splits) v += src[q * BN * rows_per];
     if (rg < p.N) y_store(p.out, int64_t(b) * p.N + rg, v, y_bias_bits(p.out, rg));
   }
 
