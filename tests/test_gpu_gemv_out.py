@@ -109,8 +109,8 @@ def test_f32_without_bias_is_nf4_gemv():
 
 @pytest.mark.parametrize("batch", [9, 16, 33, 64])
 def test_wide_batches(batch):
-    """Batches above 8 run in slabs of eight vectors (every output type, with
-    and without bias)."""
+    """Batches above 8 (the tensor-core kernel; one ragged 128-row tile, K
+    split over a cluster): every output type, with and without bias."""
     N, K = 37, 1536
     t = _quantized(870 + batch, N, K, 0.001)
     d = to_device(t)
@@ -122,6 +122,26 @@ def test_wide_batches(batch):
         assert_layer_close(y, y_ref, s_abs, dt, b, f"batch={batch} {name} + bias")
     y = gpu_gemv(t, N, K, x, d=d)
     assert_gemv_close(y, y_ref, s_abs, f"batch={batch} fp32")
+
+
+@pytest.mark.parametrize("N, K, batch, bs", [(300, 4096, 32, 64), (5100, 1024, 24, 64),
+                                             (300, 4096, 16, 256), (130, 2048, 48, 128)])
+def test_tensor_core_tiles_and_cluster_splits(N, K, batch, bs):
+    """Batches above 8 on the tensor-core kernel: several 128-row tiles with a
+    ragged last tile; K split over clusters of 8 ranks (300 x 4096 on 152 SMs),
+    2 ranks (5100 x 1024) and 4 ranks (130 x 2048); x tiles of 32 and 48 rows;
+    block sizes of 128 and 256, where one block scale spans several 64-element
+    stages."""
+    seed = 900 + N + batch
+    t = oracle.quantize(synth.weights(seed, N * K, 0.001, seed + 1), bs, 256, synth.code2_linear())
+    d = to_device(t)
+    x = synth.activations(seed + 2, batch, K)
+    y_ref, s_abs = oracle.gemv(t, N, K, x)
+    y = gpu_gemv(t, N, K, x, d=d)
+    assert_gemv_close(y, y_ref, s_abs, f"{N}x{K} batch {batch} blocksize {bs}")
+    b = synth.bias(seed + 3, N, "bf16")
+    y = gpu_gemv_ex(t, N, K, x, oracle.BF16, b, d=d)
+    assert_layer_close(y, y_ref, s_abs, oracle.BF16, b, f"{N}x{K} batch {batch} bf16 + bias")
 
 
 @pytest.mark.parametrize("layer", synth.LLAMA_7B_LAYERS, ids=lambda l: l.name)
