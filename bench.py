@@ -173,28 +173,28 @@ def run_native(args, rank, world, local_rank):
         if st:
             raise RuntimeError(f"libnf4 call failed with status {st}")
 
-    # Steps are executed in blocks of R steps (one per rotation set), kernel by
-    # kernel: R bf16 dequants, R fp16 dequants, R GEMVs, with timing events only
-    # at the phase boundaries. Each kernel therefore reads its inputs from HBM
-    # (another kernel of the same step never leaves them in L2 for it), and the
-    # per-kernel average durations come from the phase events.
+    # A graph runs S steps kernel by kernel: S bf16 dequants, S fp16 dequants,
+    # S GEMVs (step i on rotation set i mod R), with timing events only at the
+    # three phase boundaries (an event between kernels costs microseconds on
+    # this GPU; four per graph amortise over S launches each). Between two uses
+    # of one set come R - 1 other launches of the phase (over 4x L2 of other
+    # traffic), so every kernel reads its inputs from HBM; the per-kernel
+    # average durations come from the phase events.
     K, W = args.steps, args.warmup
     BLOCKS = max(1, min(4, K // R)) if K >= R else 1
 
-    def capture(nblocks, nsteps_last):
+    def capture(nsteps):
         g = torch.cuda.CUDAGraph()
         evs = []
         with torch.cuda.stream(stream):
             g.capture_begin()
-            for blk in range(nblocks):
-                steps = R if blk < nblocks - 1 else nsteps_last
-                e = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
-                e[0].record(stream)
-                for kind in range(3):
-                    for i in range(steps):
-                        launch(kind, i)
-                    e[kind + 1].record(stream)
-                evs.append((e, steps))
+            e = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+            e[0].record(stream)
+            for kind in range(3):
+                for i in range(nsteps):
+                    launch(kind, i)
+                e[kind + 1].record(stream)
+            evs.append((e, nsteps))
             g.capture_end()
         return g, evs
 
@@ -205,16 +205,12 @@ def run_native(args, rank, world, local_rank):
     stream.synchronize()
 
     S = R * BLOCKS if K >= R * BLOCKS else K
-    if K >= R * BLOCKS:
-        g_main, evs = capture(BLOCKS, R)
-    else:
-        g_main, evs = capture(1, K)
+    g_main, evs = capture(S)
     rem = K % S
     g_rem = evs_rem = None
     if rem:
-        nb_rem = (rem + R - 1) // R
         # the graph's event-record nodes refer to these events: keep them alive
-        g_rem, evs_rem = capture(nb_rem, rem - R * (nb_rem - 1))
+        g_rem, evs_rem = capture(rem)
 
     # warm-up: at least W steps
     done = 0
@@ -293,8 +289,8 @@ def run_native(args, rank, world, local_rank):
         "config": {"workload": WORKLOAD, "bytes_per_step": step_bytes,
                    "l2_policy": f"rotation over {R} distinct input/output sets "
                                 f"({R * set_bytes / 1e6:.0f} MB > 4x L2 {l2 / 1e6:.0f} MB)",
-                   "timing": f"CUDA graph of {S} steps (blocks of {R}, kernel-major within a block) "
-                             f"replayed; events only at phase boundaries",
+                   "timing": f"CUDA graph of {S} steps, kernel-major (all bf16 dequants, all fp16 "
+                             f"dequants, all GEMVs) replayed; events only at the phase boundaries",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": roofline, "detail": detail, "gpu_launches": 3 * K, "clocks": clk, "e2e": e2e,
     }
