@@ -93,7 +93,7 @@ CHAIN = [(1536, 1536, BF16, True, -1), (1536, 1536, BF16, False, 0), (8960, 1536
          (1536, 8960, F32, True, 2)]
 
 
-@pytest.mark.parametrize("batch", [1, 4])
+@pytest.mark.parametrize("batch", [1, 4, 16])
 def test_chain_parity_with_carried_error_bound(batch):
     _check_dag(CHAIN, batch, 200)
 
@@ -111,9 +111,10 @@ def _small_decoder(layers, h=512, kv=128, inter=1536):
     return spec
 
 
-@pytest.mark.parametrize("batch", [1, 2])
+@pytest.mark.parametrize("batch", [1, 2, 16])
 def test_decoder_graph_parity(batch):
-    """Two decoder layers: eight launches (q/k/v and gate/up grouped)."""
+    """Two decoder layers: eight launches (q/k/v and gate/up grouped) up to
+    batch 8; one tensor-core launch per node at batch 16."""
     _check_dag(_small_decoder(2), batch, 260)
 
 
@@ -155,7 +156,7 @@ def _decoder_nodes(layers, batch, seed):
     return nodes
 
 
-@pytest.mark.parametrize("batch", [1, 3])
+@pytest.mark.parametrize("batch", [1, 3, 24])
 def test_replays_equal_node_by_node_launches(batch):
     import w4a16_gemv_gb300 as nf4
     nodes = _decoder_nodes(2, batch, 300)
