@@ -40,6 +40,31 @@ WORKLOAD = ("nf4 4096x4096 (N(0,0.02) + 0.1% x10 outliers, blocksize 64, s2 256)
             "dequant->bf16 + dequant->fp16 + fused GEMV batch 1 (fp32 accumulate)")
 
 
+def replica_env():
+    """(world, rank, local_rank) of this process: one independent replica per
+    GPU under torch.distributed.run, else a single process."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(x, world, device=None):
+    """The largest x over all ranks (a job is as slow as its slowest replica);
+    x itself for one process."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, bytes_per_replica_step, steps, seconds):
+    """Whole-job GB/s: every replica moves bytes_per_replica_step per step;
+    `seconds` is the slowest replica's time."""
+    return world * bytes_per_replica_step * steps / seconds / 1e9
+
+
 def algorithmic_bytes():
     n = N_ROWS * K_COLS
     nb = (n + BS - 1) // BS
@@ -251,18 +276,14 @@ def run_native(args, rank, world, local_rank):
                 tot_ms += e[j].elapsed_time(e[j + 1])
                 cnt += steps
             per_kernel[name] = tot_ms / cnt * 1e3   # us per launch
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
 
     # the timed outputs are finite (a cheap guard; parity is the tests' job)
     assert torch.isfinite(sets[0]["y"]).all().item()
 
     peak, peak_src = load_peaks()
     ms_per_step = elapsed_ms / K
-    value = world * step_bytes * K / (elapsed_ms * 1e-3) / 1e9
+    value = job_throughput(world, step_bytes, K, elapsed_ms * 1e-3)
 
     detail = {}
     for name in names:
@@ -377,13 +398,16 @@ def run_e2e(args, dev, q, code2, x_host, bytes_, world):
     for _ in range(3):
         step()
     torch.cuda.synchronize()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
     t0 = time.perf_counter()
     for _ in range(steps):
         step()
     torch.cuda.synchronize()
-    dt = time.perf_counter() - t0
+    dt = max_over_ranks(time.perf_counter() - t0, world, dev)
     step_bytes = sum(bytes_.values())
-    return {"value": round(world * step_bytes * steps / dt / 1e9, 2), "unit": "GB/s",
+    return {"value": round(job_throughput(world, step_bytes, steps, dt), 2), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": round(dt / steps * 1e3, 4)}
 
@@ -821,9 +845,7 @@ def main():
     if args.steps < 1:
         raise SystemExit("--steps must be >= 1")
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local_rank = replica_env()
 
     if args.impl == "reference":
         if rank != 0:
