@@ -125,13 +125,15 @@ def test_wide_batches(batch):
 
 
 @pytest.mark.parametrize("N, K, batch, bs", [(300, 4096, 32, 64), (5100, 1024, 24, 64),
-                                             (300, 4096, 16, 256), (130, 2048, 48, 128)])
+                                             (300, 4096, 16, 256), (130, 2048, 48, 128),
+                                             (10200, 1024, 16, 64), (10200, 1024, 40, 128)])
 def test_tensor_core_tiles_and_cluster_splits(N, K, batch, bs):
     """Batches above 8 on the tensor-core kernel: several 128-row tiles with a
     ragged last tile; K split over clusters of 8 ranks (300 x 4096 on 152 SMs),
-    2 ranks (5100 x 1024) and 4 ranks (130 x 2048); x tiles of 32 and 48 rows;
-    block sizes of 128 and 256, where one block scale spans several 64-element
-    stages."""
+    2 ranks (5100 x 1024) and 4 ranks (130 x 2048); clusters of 3 ranks over
+    pairs of tiles (10200 x 1024: 80 tiles, the middle rank's stages run from
+    one tile into the next); x tiles of 32 and 48 rows; block sizes of 128 and
+    256, where one block scale spans several 64-element stages."""
     seed = 900 + N + batch
     t = oracle.quantize(synth.weights(seed, N * K, 0.001, seed + 1), bs, 256, synth.code2_linear())
     d = to_device(t)

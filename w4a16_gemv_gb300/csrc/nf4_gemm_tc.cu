@@ -58,7 +58,8 @@ struct TcArgs {
   int64_t N;
   int32_t K;
   int batch;
-  int splits;  // CTAs per cluster, along K (1, 2, 4 or 8)
+  int splits;  // CTAs per cluster (1, 2, 4 or 8 along K of one tile; 3 for a tile pair)
+  int pair;    // 1: a cluster of 3 CTAs covers two tiles (see the kernel)
   uint32_t off_b, off_w, off_recv, off_tab, off_c2, off_bar;
 };
 
@@ -177,15 +178,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int lane = tid & 31;
   const int kq = warp >> 2;                 // K quarter of a stage (16 elements)
   const int row = (warp & 3) * 32 + lane;   // row of the tile = TMEM lane
-  const int tile = int(blockIdx.x) / p.splits;
-  const int split = int(blockIdx.x) - tile * p.splits;  // rank in the cluster
+  const int cl = int(blockIdx.x) / p.splits;
+  const int split = int(blockIdx.x) - cl * p.splits;  // rank in the cluster
   const QuantTensor& t = p.t;
   const int64_t K = p.K;
   const int S = int(K / kStageK);
+  // The CTA's work is a range of consecutive (tile, stage) units: split
+  // `split` of the stages of tile `cl`, or, for a tile pair, a third of the
+  // 2S units of tiles 2 cl and 2 cl + 1. Its units i < ib are stages s0 + i
+  // of tile `tile`; units i >= ib (the middle rank of a pair only) are
+  // stages i - ib of tile + 1.
+  int tile, s0, ns, ib;
+  if (p.pair) {
+    const int u0 = int(int64_t(split) * 2 * S / 3), u1 = int(int64_t(split + 1) * 2 * S / 3);
+    tile = 2 * cl + (u0 >= S ? 1 : 0);
+    s0 = u0 >= S ? u0 - S : u0;
+    ns = u1 - u0;
+    ib = (u0 < S && u1 > S) ? S - u0 : ns;
+  } else {
+    tile = cl;
+    s0 = int(int64_t(split) * S / p.splits);
+    ns = int(int64_t(split + 1) * S / p.splits) - s0;
+    ib = ns;
+  }
   const int64_t r_glob = int64_t(tile) * kTileM + row;
   const bool row_ok = r_glob < p.N;
-  const int s0 = int(int64_t(split) * S / p.splits);
-  const int ns = int(int64_t(split + 1) * S / p.splits) - s0;
+  const bool row_ok_b = r_glob + kTileM < p.N;  // the same row of the second tile
 
   const uint32_t sbase = smem_u32(smem);
   const uint32_t b_ring = sbase + p.off_b;                    // kRing slots of BN x 128 B
@@ -231,8 +249,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   auto load_scale_in = [&](int i, uint32_t& q, uint32_t& a2) {
     q = 0u;
     a2 = 0u;
-    if (producer && i < ns && row_ok) {
-      const int64_t blk = (r_glob * K + int64_t(s0 + i) * kStageK) >> t.lbs;
+    const bool second = i >= ib;
+    if (producer && i < ns && (second ? row_ok_b : row_ok)) {
+      const int64_t e = second ? (r_glob + kTileM) * K + int64_t(i - ib) * kStageK
+                               : r_glob * K + int64_t(s0 + i) * kStageK;
+      const int64_t blk = e >> t.lbs;
       q = __ldg(t.absmax_q + blk);
       a2 = __ldg(t.absmax2 + (blk >> t.ls2));
     }
@@ -244,10 +265,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // kTcThreads - 32 only).
   auto issue_tiles = [&](int i) {
     const int slot = i % kRing;
+    const bool second = i >= ib;
+    const int st = second ? i - ib : s0 + i;  // stage within its tile
     mbar_arrive_expect_tx(&full[slot], uint32_t(kTileM * kStageK / 2 + BN * 128));
-    tma_load_2d(w_ring + uint32_t(slot) * 4096u, &tmw, (s0 + i) * (kStageK / 2), tile * kTileM,
+    tma_load_2d(w_ring + uint32_t(slot) * 4096u, &tmw, st * (kStageK / 2), (tile + (second ? 1 : 0)) * kTileM,
                 &full[slot]);
-    tma_load_2d(b_ring + uint32_t(slot) * uint32_t(BN * 128), &tmx, (s0 + i) * kStageK, 0, &full[slot]);
+    tma_load_2d(b_ring + uint32_t(slot) * uint32_t(BN * 128), &tmx, st * kStageK, 0, &full[slot]);
   };
 
   __syncthreads();  // barriers initialised before any copy uses one
@@ -300,8 +323,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           ok = mbar_wait_bounded(&full[u], ph, kWaitLimitCycles) && ok;
 
           // block scale fp32(fp32(code2[q] * absmax2[g]) + offset); 0 past the last row
-          const float sc =
-              row_ok ? __fadd_rn(__fmul_rn(sC2[qv[u]], half_bits_to_float(uint16_t(av[u]))), t.offset) : 0.0f;
+          const float sc = (i >= ib ? row_ok_b : row_ok)
+                               ? __fadd_rn(__fmul_rn(sC2[qv[u]], half_bits_to_float(uint16_t(av[u]))), t.offset)
+                               : 0.0f;
           load_scale_in(i + kRing, qv[u], av[u]);
           if (u < kRing - kNA && i0 == 0) load_scale_in(u + kNA, qv[u + kNA], av[u + kNA]);
           const float2 sc2 = make_float2(sc, sc);
@@ -351,12 +375,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tc_fence_after();
           const uint32_t a_t = tbase + uint32_t(u % kNA) * 64u;
           const uint64_t bd = desc0 + uint64_t(u * kSlotUnits);
-          mma_bf16(d_col, a_t, bd, kIdesc, (i0 + u) > 0 ? 1u : 0u);
-          mma_bf16(d_col, a_t + 32u, bd, kIdesc, 1u);
+          // the second tile's units accumulate into their own columns
+          const int i = i0 + u;
+          const uint32_t dc = d_col + (i >= ib ? uint32_t(BN) : 0u);
+          mma_bf16(dc, a_t, bd, kIdesc, (i > 0 && i != ib) ? 1u : 0u);
+          mma_bf16(dc, a_t + 32u, bd, kIdesc, 1u);
 #pragma unroll
           for (int j = 1; j < kStageK / 16; ++j) {  // 32 bytes of K per step
-            mma_bf16(d_col, a_t + 8u * uint32_t(j), bd + uint64_t(2 * j), kIdesc, 1u);
-            mma_bf16(d_col, a_t + 32u + 8u * uint32_t(j), bd + uint64_t(2 * j), kIdesc, 1u);
+            mma_bf16(dc, a_t + 8u * uint32_t(j), bd + uint64_t(2 * j), kIdesc, 1u);
+            mma_bf16(dc, a_t + 32u + 8u * uint32_t(j), bd + uint64_t(2 * j), kIdesc, 1u);
           }
           tc_commit(&mdone[u]);  // frees A buffer u % kNA and ring slot u
         }
@@ -380,57 +407,118 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_after();
   asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // every peer is running
 
-  // Split-K: the CTA owning rows [rank * R, (rank + 1) * R) of the tile (R
-  // = 128 / splits) receives every rank's partial sums of those rows in its
-  // own receive buffer (not used before, so peers may write as soon as their
-  // MMAs are done); warp (row quarter, K quarter kq) pushes columns
-  // [kq * BN / 4, (kq + 1) * BN / 4) of its lanes' rows.
-  const int rows_per = kTileM / p.splits;
-  {
-    const int owner = row / rows_per;
-    const int rl = row - owner * rows_per;
-    uint32_t dst = smem_u32(recv) + uint32_t((split * BN) * rows_per + rl) * 4u;
-    asm volatile("mapa.shared::cluster.u32 %0, %0, %1;" : "+r"(dst) : "r"(uint32_t(owner)));
-    if (producer) {
-      // all BN / 4 columns of this warp's quarter, then one wait
+  if (p.pair) {
+    // Tile pair: rank 0 owns tile 2 cl, rank 2 owns tile 2 cl + 1; the
+    // middle rank pushes its partial sums of both tiles (its two
+    // accumulators) into the owners' receive buffers, laid out [BN][128].
+    // After one cluster barrier each owner adds its own accumulator (two
+    // terms, so the order of the operands does not matter) and applies the
+    // output stage. Warp (row quarter, K quarter kq) handles columns
+    // [kq * BN / 4, (kq + 1) * BN / 4) of its lanes' rows.
+    if (split == 1 && producer) {
+#pragma unroll
+      for (int seg = 0; seg < 2; ++seg) {
+        uint32_t dst = smem_u32(recv) + uint32_t(row) * 4u;
+        asm volatile("mapa.shared::cluster.u32 %0, %0, %1;" : "+r"(dst) : "r"(uint32_t(seg == 0 ? 0 : 2)));
+        uint32_t v[BN / 4];
+#pragma unroll
+        for (int c0 = 0; c0 < BN / 4; c0 += 4) {
+          uint32_t w4[4];
+          tmem_ld4(lane_base + 64u * kNA + uint32_t(seg * BN + kq * (BN / 4) + c0), w4);
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) v[c0 + jj] = w4[jj];
+        }
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+        for (int jj = 0; jj < BN / 4; ++jj) asm volatile("" : "+r"(v[jj]));  // uses follow the wait
+#pragma unroll
+        for (int jj = 0; jj < BN / 4; ++jj) {
+          const int n = kq * (BN / 4) + jj;
+          const float f = ok ? __uint_as_float(v[jj]) : __uint_as_float(0x7fc00000u);
+          asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dst + uint32_t(n * kTileM) * 4u), "f"(f)
+                       : "memory");
+        }
+      }
+    }
+    if (!ok) atomicOr(&g_tc_flags, 1u);
+    cluster_sync();  // the middle rank's pushes have landed
+    if (split != 1 && producer) {
       uint32_t v[BN / 4];
 #pragma unroll
       for (int c0 = 0; c0 < BN / 4; c0 += 4) {
         uint32_t w4[4];
         tmem_ld4(lane_base + 64u * kNA + uint32_t(kq * (BN / 4) + c0), w4);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) v[c0 + j] = w4[j];
+        for (int jj = 0; jj < 4; ++jj) v[c0 + jj] = w4[jj];
       }
       asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-      for (int j = 0; j < BN / 4; ++j) asm volatile("" : "+r"(v[j]));  // uses follow the wait
+      for (int jj = 0; jj < BN / 4; ++jj) asm volatile("" : "+r"(v[jj]));  // uses follow the wait
+      if (row_ok) {
+        const uint32_t bias_bits = y_bias_bits(p.out, r_glob);
 #pragma unroll
-      for (int j = 0; j < BN / 4; ++j) {
-        const int n = kq * (BN / 4) + j;
-        const float f = ok ? __uint_as_float(v[j]) : __uint_as_float(0x7fc00000u);
-        asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dst + uint32_t(n * rows_per) * 4u), "f"(f)
-                     : "memory");
+        for (int jj = 0; jj < BN / 4; ++jj) {
+          const int n = kq * (BN / 4) + jj;
+          if (n < p.batch) {
+            const float own = ok ? __uint_as_float(v[jj]) : __uint_as_float(0x7fc00000u);
+            y_store(p.out, int64_t(n) * p.N + r_glob, own + recv[n * kTileM + row], bias_bits);
+          }
+        }
       }
     }
-  }
-  if (!ok) atomicOr(&g_tc_flags, 1u);
-  cluster_sync();  // every rank's pushes have landed
+  } else {
+    // Split-K: the CTA owning rows [rank * R, (rank + 1) * R) of the tile (R
+    // = 128 / splits) receives every rank's partial sums of those rows in its
+    // own receive buffer (not used before, so peers may write as soon as their
+    // MMAs are done); warp (row quarter, K quarter kq) pushes columns
+    // [kq * BN / 4, (kq + 1) * BN / 4) of its lanes' rows.
+    const int rows_per = kTileM / p.splits;
+    {
+      const int owner = row / rows_per;
+      const int rl = row - owner * rows_per;
+      uint32_t dst = smem_u32(recv) + uint32_t((split * BN) * rows_per + rl) * 4u;
+      asm volatile("mapa.shared::cluster.u32 %0, %0, %1;" : "+r"(dst) : "r"(uint32_t(owner)));
+      if (producer) {
+        // all BN / 4 columns of this warp's quarter, then one wait
+        uint32_t v[BN / 4];
+  #pragma unroll
+        for (int c0 = 0; c0 < BN / 4; c0 += 4) {
+          uint32_t w4[4];
+          tmem_ld4(lane_base + 64u * kNA + uint32_t(kq * (BN / 4) + c0), w4);
+  #pragma unroll
+          for (int j = 0; j < 4; ++j) v[c0 + j] = w4[j];
+        }
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  #pragma unroll
+        for (int j = 0; j < BN / 4; ++j) asm volatile("" : "+r"(v[j]));  // uses follow the wait
+  #pragma unroll
+        for (int j = 0; j < BN / 4; ++j) {
+          const int n = kq * (BN / 4) + j;
+          const float f = ok ? __uint_as_float(v[j]) : __uint_as_float(0x7fc00000u);
+          asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dst + uint32_t(n * rows_per) * 4u), "f"(f)
+                       : "memory");
+        }
+      }
+    }
+    if (!ok) atomicOr(&g_tc_flags, 1u);
+    cluster_sync();  // every rank's pushes have landed
 
-  // Rows [split * R, (split + 1) * R): the sum over ranks in rank order,
-  // then the output stage.
-  const int lrp = 31 - __clz(rows_per);  // rows_per is a power of two
-  const int total = rows_per * p.batch;
-  const int64_t rg0 = int64_t(tile) * kTileM + split * rows_per;
-  for (int e = tid; e < total; e += kTcThreads) {
-    const int b = e >> lrp;
-    const int rl = e & (rows_per - 1);
-    const int64_t rg = rg0 + rl;
-    const float* src = recv + b * rows_per + rl;
-    float v = src[0];
-#pragma unroll
-    for (int q = 1; q < 8; ++q)
-      if (q < p.splits) v += src[q * BN * rows_per];
-    if (rg < p.N) y_store(p.out, int64_t(b) * p.N + rg, v, y_bias_bits(p.out, rg));
+    // Rows [split * R, (split + 1) * R): the sum over ranks in rank order,
+    // then the output stage.
+    const int lrp = 31 - __clz(rows_per);  // rows_per is a power of two
+    const int total = rows_per * p.batch;
+    const int64_t rg0 = int64_t(tile) * kTileM + split * rows_per;
+    for (int e = tid; e < total; e += kTcThreads) {
+      const int b = e >> lrp;
+      const int rl = e & (rows_per - 1);
+      const int64_t rg = rg0 + rl;
+      const float* src = recv + b * rows_per + rl;
+      float v = src[0];
+  #pragma unroll
+      for (int q = 1; q < 8; ++q)
+        if (q < p.splits) v += src[q * BN * rows_per];
+      if (rg < p.N) y_store(p.out, int64_t(b) * p.N + rg, v, y_bias_bits(p.out, rg));
+    }
   }
 
   tc_fence_before();
@@ -504,7 +592,11 @@ cudaError_t try_gemm_tc(const QuantTensor& t, int64_t N, int64_t K, const uint16
   int splits = 1;
   while (splits < 8 && (S + splits - 1) / splits > kLongStages) splits *= 2;
   while (splits < 8 && tiles * splits * 2 <= sms && S / (splits * 2) >= 4) splits *= 2;
-  const int grid = int(tiles) * splits;
+  // One CTA per tile leaving more than a third of the SMs idle: clusters of
+  // three CTAs over pairs of tiles (two thirds of a tile's stages each).
+  const bool pair = splits == 1 && tiles % 2 == 0 && tiles * 3 / 2 <= sms && tiles * 3 < int64_t(sms) * 2 &&
+                    S >= 6;
+  const int grid = pair ? int(tiles / 2) * 3 : int(tiles) * splits;
 
   TcArgs a;
   a.t = t;
@@ -513,7 +605,8 @@ cudaError_t try_gemm_tc(const QuantTensor& t, int64_t N, int64_t K, const uint16
   a.N = N;
   a.K = int32_t(K);
   a.batch = batch;
-  a.splits = splits;
+  a.splits = pair ? 3 : splits;
+  a.pair = pair ? 1 : 0;
   // Shared memory, from a 1024-aligned base: [weight ring | code2 |
   // barriers | pair table | x ring | split-K receive buffer].
   a.off_w = 0;
