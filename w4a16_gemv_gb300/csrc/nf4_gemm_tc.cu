@@ -1,4 +1,4 @@
-// nf4_gemm_tc.cu -- the fused GEMV for wide batches (16..64 vectors) on the
+// nf4_gemm_tc.cu -- the fused GEMV for wide batches (9..64 vectors) on the
 // 5th-generation tensor cores: y = W_hat x with the dequantization fused.
 //
 // At these batches the contraction is dense ("CUDA 进阶手册 / 量化与 GEMV",
@@ -19,11 +19,14 @@
 //   * one warp issues tcgen05.mma (kind::f16, bf16 x bf16 -> fp32 in TMEM),
 //     two per 16-element K step (hi and lo), once the producer warps have
 //     signalled the stage's A buffer full; its commit frees the A buffer and
-//     the ring slot, which another warp refills with the tile copies. The producers run
-//     up to four stages ahead of the MMAs (four A buffers in TMEM);
-//   * K is split over a thread-block cluster; partial sums are added in rank
-//     order through distributed shared memory (deterministic) and the output
-//     stage (bias, rounding to y's type) is applied once.
+//     the ring slot, which another warp refills with the tile copies. The
+//     producers run up to four stages ahead of the MMAs (four A buffers in
+//     TMEM);
+//   * K is split over a thread-block cluster; each CTA pushes its partial
+//     sums into the shared memory of the rank that owns the rows, which adds
+//     them in rank order (deterministic) and applies the output stage (bias,
+//     rounding to y's type) once. When one CTA per tile would leave many SMs
+//     idle, a cluster of three CTAs covers a pair of tiles instead.
 // Every wait on an mbarrier is bounded (about one second); a wait that runs
 // out sets bit 0 of the device error flags and the kernel still completes
 // its cluster barriers and frees its tensor memory.
