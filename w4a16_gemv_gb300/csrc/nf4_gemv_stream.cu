@@ -752,14 +752,18 @@ __device__ __forceinline__ float2 lds_f2(uint32_t addr) {
 }
 
 // One step (rows r0 .. r0 + rows - 1 of the CTA): per row and vector, the
-// lane's dot product times the block scale; transposed warp reduction over
-// the RPG * BP values; partial added to (or stored in, for the first slice)
+// lane's dot product; transposed warp reduction over the RPG * BP values,
+// with the block scale applied once the lanes of one quantization block
+// (32 / CB adjacent lanes: blocks of at least 64 elements) have been summed;
+// partial added to (or stored in, for the first slice)
 // sPart[(row * BP + vector) * W + warp].
 template <int BP, int CB, int RPG>
 __device__ __forceinline__ void compute_step_n(const Step<CB, RPG>& st, const LaneN<BP, CB>& L,
                                                const float* sScale, float* sPart, int spr, int W,
                                                int wg, int lane, int r0, int rows, bool first) {
-  float part[RPG * BP];
+  static_assert(RPG == 2 && BP * CB == 32, "two rows; 32 / CB lanes cover 64 elements");
+  constexpr int V = RPG * BP;
+  float part[V];
 #pragma unroll
   for (int r = 0; r < RPG; ++r) {
     float2 acc[BP];
@@ -778,12 +782,42 @@ __device__ __forceinline__ void compute_step_n(const Step<CB, RPG>& st, const La
         }
       }
     }
-    const bool keep = L.act && r < rows;
-    const float sc = sScale[(r0 + (r < rows ? r : 0)) * spr + L.scol];
 #pragma unroll
-    for (int b = 0; b < BP; ++b) part[r * BP + b] = keep ? sc * (acc[b].x + acc[b].y) : 0.0f;
+    for (int b = 0; b < BP; ++b) part[r * BP + b] = acc[b].x + acc[b].y;  // lanes past the row have x = 0
   }
-  const float red = transposed_warp_reduce<RPG * BP>(part, lane);
+  // Transposed steps over the lanes of one block (masks 1 .. 16 / CB): the
+  // first step sends row 1 to the odd lanes; afterwards a lane holds two
+  // values of row (lane & 1), summed over its block's lanes.
+  constexpr int kPre = CB == 4 ? 3 : CB == 8 ? 2 : 1;
+#pragma unroll
+  for (int step = 0; step < kPre; ++step) {
+    const int cnt = V >> step;
+    const int m = 1 << step;
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int i = 0; i < cnt / 2; ++i) {
+      const float send = upper ? part[i] : part[i + cnt / 2];
+      const float keep = upper ? part[i + cnt / 2] : part[i];
+      part[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+    }
+  }
+  {
+    const int r = lane & 1;  // rows past the end (stale registers) get scale 0
+    const float sc = r < rows ? sScale[(r0 + r) * spr + L.scol] : 0.0f;
+    part[0] *= sc;
+    part[1] *= sc;
+  }
+  // the last transposed step, then plain butterfly steps over the blocks
+  float red;
+  {
+    const int m = 1 << kPre;
+    const bool upper = (lane & m) != 0;
+    const float send = upper ? part[0] : part[1];
+    const float keep = upper ? part[1] : part[0];
+    red = keep + __shfl_xor_sync(0xffffffffu, send, m);
+  }
+#pragma unroll
+  for (int m = 2 << kPre; m < 32; m <<= 1) red += __shfl_xor_sync(0xffffffffu, red, m);
   if (lane < RPG * BP) {
     const int idx = transposed_index<RPG * BP>(lane);
     const int r = idx / BP, b = idx - (idx / BP) * BP;
@@ -1006,7 +1040,9 @@ bool plan_bn(const SubTensor* subs, int nsub, int64_t K, const uint16_t* x, int 
   const QuantTensor& t = subs[0].t;
   const int64_t bs = int64_t(1) << t.lbs;
   const int ce = 2 * cb;
-  if (K % 32 != 0 || K % bs != 0 || bs < ce) return false;
+  // blocks of at least 64 elements: a block's lanes are adjacent groups of
+  // 32 / cb lanes (the scale is applied inside the warp reduction)
+  if (K % 32 != 0 || K % bs != 0 || bs < 64) return false;
   const int64_t cpr = K / ce;
   int W = int((cpr + 31) / 32);
   int slices = 1;
