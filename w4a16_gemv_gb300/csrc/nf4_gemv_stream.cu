@@ -761,8 +761,13 @@ template <int BP, int CB, int RPG>
 __device__ __forceinline__ void compute_step_n(const Step<CB, RPG>& st, const LaneN<BP, CB>& L,
                                                const float* sScale, float* sPart, int spr, int W,
                                                int wg, int lane, int r0, int rows, bool first) {
-  static_assert(RPG == 2 && BP * CB == 32, "two rows; 32 / CB lanes cover 64 elements");
   constexpr int V = RPG * BP;
+  // lanes of one 64-element block: 32 / CB (2^kPre); log2(V) transposed steps
+  constexpr int kPre = CB == 4 ? 3 : CB == 8 ? 2 : 1;
+  constexpr int kSteps = V == 4 ? 2 : V == 8 ? 3 : 4;
+  static_assert(RPG == 2 && (CB == 4 || CB == 8 || CB == 16) && (V == 4 || V == 8 || V == 16) &&
+                    kPre < kSteps,
+                "two rows per step; the block's lanes are summed before the last transposed step");
   float part[V];
 #pragma unroll
   for (int r = 0; r < RPG; ++r) {
@@ -785,12 +790,12 @@ __device__ __forceinline__ void compute_step_n(const Step<CB, RPG>& st, const La
 #pragma unroll
     for (int b = 0; b < BP; ++b) part[r * BP + b] = acc[b].x + acc[b].y;  // lanes past the row have x = 0
   }
-  // Transposed steps over the lanes of one block (masks 1 .. 16 / CB): the
-  // first step sends row 1 to the odd lanes; afterwards a lane holds two
-  // values of row (lane & 1), summed over its block's lanes.
-  constexpr int kPre = CB == 4 ? 3 : CB == 8 ? 2 : 1;
-#pragma unroll
-  for (int step = 0; step < kPre; ++step) {
+  // Transposed steps: the first sends row 1 to the odd lanes; after the
+  // steps over the lanes of one block (masks 1 .. 16 / CB) a lane holds
+  // V >> kPre values of row (lane & 1), summed over its block's lanes, which
+  // take the block scale; the remaining steps and plain butterfly steps
+  // combine the blocks.
+  auto exchange = [&](int step) {
     const int cnt = V >> step;
     const int m = 1 << step;
     const bool upper = (lane & m) != 0;
@@ -800,24 +805,20 @@ __device__ __forceinline__ void compute_step_n(const Step<CB, RPG>& st, const La
       const float keep = upper ? part[i + cnt / 2] : part[i];
       part[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
     }
-  }
+  };
+#pragma unroll
+  for (int step = 0; step < kPre; ++step) exchange(step);
   {
     const int r = lane & 1;  // rows past the end (stale registers) get scale 0
     const float sc = r < rows ? sScale[(r0 + r) * spr + L.scol] : 0.0f;
-    part[0] *= sc;
-    part[1] *= sc;
-  }
-  // the last transposed step, then plain butterfly steps over the blocks
-  float red;
-  {
-    const int m = 1 << kPre;
-    const bool upper = (lane & m) != 0;
-    const float send = upper ? part[0] : part[1];
-    const float keep = upper ? part[1] : part[0];
-    red = keep + __shfl_xor_sync(0xffffffffu, send, m);
+#pragma unroll
+    for (int i = 0; i < (V >> kPre); ++i) part[i] *= sc;
   }
 #pragma unroll
-  for (int m = 2 << kPre; m < 32; m <<= 1) red += __shfl_xor_sync(0xffffffffu, red, m);
+  for (int step = kPre; step < kSteps; ++step) exchange(step);
+  float red = part[0];
+#pragma unroll
+  for (int m = V; m < 32; m <<= 1) red += __shfl_xor_sync(0xffffffffu, red, m);
   if (lane < RPG * BP) {
     const int idx = transposed_index<RPG * BP>(lane);
     const int r = idx / BP, b = idx - (idx / BP) * BP;
@@ -869,9 +870,10 @@ struct BNArgs {
   uint32_t off_c2, off_a2, off_q, off_scale, off_part, off_bias, off_tab;
 };
 
-template <int BP, int CB, int RPG, int NSUB>
-__global__ void __launch_bounds__(512, 1) gemv_bn_kernel(const BNArgs p) {
-  constexpr int kThreads = 512;
+template <int BP, int CB, int RPG, int NSUB, int NT>
+__global__ void __launch_bounds__(NT, 1) gemv_bn_kernel(const BNArgs p) {
+  constexpr int kThreads = NT;
+  static_assert(NT >= 256 && NT % 32 == 0, "the prologue loads assume at least 256 threads");
   constexpr int CE = 2 * CB;
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x;
@@ -1034,9 +1036,10 @@ __global__ void __launch_bounds__(512, 1) gemv_bn_kernel(const BNArgs p) {
   }
 }
 
-// Plan for BP vectors and CB-byte chunks (512 threads, one CTA per SM).
+// Plan for BP vectors, CB-byte chunks and nt threads (one CTA per SM).
 bool plan_bn(const SubTensor* subs, int nsub, int64_t K, const uint16_t* x, int batch, int bp,
-             int cb, int sms, BNArgs* p, int* grid, uint32_t* smem_bytes) {
+             int cb, int nt, int sms, BNArgs* p, int* grid, uint32_t* smem_bytes) {
+  const int warps = nt / 32;
   const QuantTensor& t = subs[0].t;
   const int64_t bs = int64_t(1) << t.lbs;
   const int ce = 2 * cb;
@@ -1046,11 +1049,11 @@ bool plan_bn(const SubTensor* subs, int nsub, int64_t K, const uint16_t* x, int 
   const int64_t cpr = K / ce;
   int W = int((cpr + 31) / 32);
   int slices = 1;
-  if (W > 16) {
-    slices = int((W + 15) / 16);
+  if (W > warps) {
+    slices = int((W + warps - 1) / warps);
     W = int((cpr + 32 * slices - 1) / (32 * slices));
   }
-  int G = 16 / W;
+  int G = warps / W;
   if (G > kMaxGroups) G = kMaxGroups;
   const int max_rows = assign_ctas(subs, nsub, sms, p->sub, grid);
   if (max_rows <= 0) return false;
@@ -1066,7 +1069,7 @@ bool plan_bn(const SubTensor* subs, int nsub, int64_t K, const uint16_t* x, int 
   if (slices > 1) G = 1;
   p->G = G;
   const int64_t max_nq = int64_t(max_rows) * p->spr;
-  if (max_nq > int64_t(4) * 512 * 16) return false;
+  if (max_nq > int64_t(4) * nt * 16) return false;
   const int ng_cap = int((max_nq >> t.ls2) + 2);
   const int res = reserved_smem_per_block();
   if (res <= 0 || res >= 65536 || res % 256 != 0) return false;
@@ -1104,19 +1107,19 @@ cudaError_t set_smem_limit_once(Kern kern, int* attr_set) {
   return cudaSuccess;
 }
 
-template <int BP, int CB, int NSUB>
+template <int BP, int CB, int NSUB, int NT>
 cudaError_t launch_bn(const BNArgs& a, int grid, uint32_t smem_bytes, cudaStream_t stream) {
-  auto kern = gemv_bn_kernel<BP, CB, 2, NSUB>;
+  auto kern = gemv_bn_kernel<BP, CB, 2, NSUB, NT>;
   static int attr_set[64] = {0};
   const cudaError_t e = set_smem_limit_once(kern, attr_set);
   if (e != cudaSuccess) return e;
-  return launch_k(kern, dim3(unsigned(grid)), dim3(512u), smem_bytes, stream, a);
+  return launch_k(kern, dim3(unsigned(grid)), dim3(unsigned(NT)), smem_bytes, stream, a);
 }
 
-template <int BP, int CB>
+template <int BP, int CB, int NT>
 cudaError_t launch_bn_n(const BNArgs& a, int grid, uint32_t smem_bytes, cudaStream_t stream) {
-  return a.nsub == 1 ? launch_bn<BP, CB, 1>(a, grid, smem_bytes, stream)
-                     : launch_bn<BP, CB, kMaxSub>(a, grid, smem_bytes, stream);
+  return a.nsub == 1 ? launch_bn<BP, CB, 1, NT>(a, grid, smem_bytes, stream)
+                     : launch_bn<BP, CB, kMaxSub, NT>(a, grid, smem_bytes, stream);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -1152,23 +1155,26 @@ cudaError_t try_gemv_bn(const SubTensor* subs, int nsub, int64_t K, const uint16
   if (batch < 2 || batch > 8 || !aligned16(x)) return cudaSuccess;
   for (int j = 0; j < nsub; ++j)
     if (!aligned16(subs[j].t.packed)) return cudaSuccess;
-  // x chunk of all BP vectors in registers: BP * 2 CB binary32 values = 64
+  // x chunk of all BP vectors in registers: BP * 2 CB binary32 values, 64
+  // on 512 threads or 128 on 256
   BNArgs a;
   int grid = 0;
   uint32_t smem = 0;
   if (batch == 2) {
-    if (!plan_bn(subs, nsub, K, x, batch, 2, 16, sms, &a, &grid, &smem)) return cudaSuccess;
+    if (!plan_bn(subs, nsub, K, x, batch, 2, 16, 512, sms, &a, &grid, &smem)) return cudaSuccess;
     *done = true;
-    return launch_bn_n<2, 16>(a, grid, smem, stream);
+    return launch_bn_n<2, 16, 512>(a, grid, smem, stream);
   }
   if (batch <= 4) {
-    if (!plan_bn(subs, nsub, K, x, batch, 4, 8, sms, &a, &grid, &smem)) return cudaSuccess;
+    if (!plan_bn(subs, nsub, K, x, batch, 4, 8, 512, sms, &a, &grid, &smem)) return cudaSuccess;
     *done = true;
-    return launch_bn_n<4, 8>(a, grid, smem, stream);
+    return launch_bn_n<4, 8, 512>(a, grid, smem, stream);
   }
-  if (!plan_bn(subs, nsub, K, x, batch, 8, 4, sms, &a, &grid, &smem)) return cudaSuccess;
+  // 5..8 vectors: 8-byte chunks (128 binary32 x values per lane) on 256
+  // threads, half the reduction work per weight of 4-byte chunks on 512
+  if (!plan_bn(subs, nsub, K, x, batch, 8, 8, 256, sms, &a, &grid, &smem)) return cudaSuccess;
   *done = true;
-  return launch_bn_n<8, 4>(a, grid, smem, stream);
+  return launch_bn_n<8, 8, 256>(a, grid, smem, stream);
 }
 
 
