@@ -50,7 +50,7 @@ constexpr int kRing = 8;         // stages of packed weights and x in shared mem
 constexpr int kAhead = kRing - 2;  // stages loaded ahead of the one being dequantized
 constexpr int kLongStages = 64;  // stages per CTA above which K is split further
 constexpr int kNA = 4;               // A buffers in TMEM (the producers' lead over the MMAs)
-constexpr uint32_t kTmemCols = 512;  // A: kNA buffers x 64 columns (hi 32 + lo 32); D: 256..319
+constexpr uint32_t kTmemCols = 512;  // A: kNA x 64 columns (hi 32 + lo 32); D: from 256, BN (x 2 for a pair)
 
 __device__ unsigned int g_tc_flags = 0;  // bit 0: an mbarrier wait ran out
 
@@ -361,10 +361,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else if (warp == kMmaWarp && lane == 0) {
     // MMA issue. One thread, sharing its scheduler with producer warps: the
-    // per-stage instruction stream is kept short (ring and buffer indices
-    // and phases advance incrementally; the x-tile descriptor of a slot and
-    // K step is the slot-0 descriptor plus a constant in its 16-byte address
-    // field).
+    // per-stage instruction stream is kept short (the loop is unrolled over
+    // the ring, so slots, A buffers and phases are compile-time constants;
+    // the x-tile descriptor of a slot and K step is the slot-0 descriptor
+    // plus a constant in its 16-byte address field). One wait per stage: the
+    // producers signal the A buffer only after the stage's tiles landed.
     const uint64_t desc0 = desc_sw128(b_ring);
     constexpr uint32_t kSlotUnits = uint32_t(BN * 128) >> 4;
     static_assert(kRing % kNA == 0, "ring slots and A buffers advance together");
