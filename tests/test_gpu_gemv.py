@@ -73,6 +73,20 @@ def test_block_sizes(bs, s2):
         assert_gemv_close(y, y_ref, s_abs, f"bs={bs} s2={s2} batch={batch}")
 
 
+@pytest.mark.parametrize("K, bs, batch, x_offset", [(1040, 16, 12, 0), (70, 2, 9, 0),
+                                                    (1536, 32, 20, 0), (1536, 64, 17, 1)])
+def test_wide_batches_in_slabs(K, bs, batch, x_offset):
+    """Batches above 8 that the tensor-core kernel does not take (K not a
+    multiple of 64, block sizes below 64, x not 16-byte aligned) run as slabs
+    of at most eight vectors through the CUDA-core kernels."""
+    N = 45
+    t = oracle.quantize(synth.weights(1000 + K, N * K, 0.001, 1001), bs, 256, synth.code2_linear())
+    x = synth.activations(1002 + batch, batch, K)
+    y = gpu_gemv(t, N, K, x, x_offset=x_offset)
+    y_ref, s_abs = oracle.gemv(t, N, K, x)
+    assert_gemv_close(y, y_ref, s_abs, f"K={K} bs={bs} batch={batch} x_offset={x_offset}")
+
+
 def test_ragged_k_blocks_straddle_rows():
     """K = 1000 is not a multiple of 64: blocks straddle rows (generic kernel)."""
     N, K = 33, 1000
