@@ -291,6 +291,8 @@ def run_native(args, rank, world, local_rank):
         if us:
             gbs = bytes_[name] / (us * 1e-6) / 1e9
             d = {"us": round(us, 3), "gbs": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peak, 4)}
+            if name.startswith("dequant"):
+                d["gelem_per_s"] = round(N_ROWS * K_COLS / (us * 1e-6) / 1e9, 2)
             if name.startswith("gemv"):
                 d["us_per_layer"] = d.pop("us")
             detail[name] = d
@@ -709,6 +711,7 @@ def run_sweep(args):
         gbs = bytes_ / us / 1e3
         out.append({"kind": "dequant", "case": name, "out": "bf16" if dtype == 0 else "fp16", "n": n,
                     "bytes": bytes_, "us": round(us, 3), "gbs": round(gbs, 1),
+                    "gelem_per_s": round(n / us / 1e3, 2),
                     "frac_of_measured_hbm": round(gbs / peak, 4), "frac_of_8000": round(gbs / 8000.0, 4),
                     "sets": r})
         del sets
