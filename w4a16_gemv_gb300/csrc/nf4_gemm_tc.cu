@@ -211,7 +211,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t sbase = smem_u32(smem);
   const uint32_t b_ring = sbase + p.off_b;                    // kRing slots of BN x 128 B
   const uint32_t w_ring = sbase + p.off_w;                    // kRing slots of 4 KB
-  float* recv = reinterpret_cast<float*>(smem + p.off_recv);  // [src rank][BN][128 / splits]
+  // partial sums received from peers: [src rank][BN][128 / splits] along K,
+  // [BN][128] from the middle rank of a tile pair
+  float* recv = reinterpret_cast<float*>(smem + p.off_recv);
   float* sC2 = reinterpret_cast<float*>(smem + p.off_c2);
   uint64_t* afull = reinterpret_cast<uint64_t*>(smem + p.off_bar);  // A buffer written (16 warps)
   uint64_t* mdone = afull + kNA;  // MMAs of a stage done (frees its A buffer and ring slot), per slot
@@ -296,10 +298,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   }
   if (tid < 256) sC2[tid] = half_bits_to_float(c2v);
-  __syncthreads();  // sC2 ready
 
   tc_fence_before();
-  __syncthreads();
+  __syncthreads();  // pair table, sC2 and the TMEM address ready
   tc_fence_after();
   const uint32_t tbase = *s_taddr;
   const uint32_t lane_base = tbase + (uint32_t((warp & 3) * 32) << 16);
