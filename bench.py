@@ -359,7 +359,10 @@ def read_traffic(kernel_name):
 
 def run_e2e(args, dev, q, code2, x_host, bytes_, world):
     """Same step through the public API with host buffers: H2D of the step's
-    inputs from pinned memory and D2H of its outputs inside the timed region."""
+    inputs from pinned memory and D2H of its outputs inside the timed region.
+    Steps are pipelined as a caller would: the two dequant outputs go back to
+    the host on two copy streams while the next step's inputs come in and its
+    kernels run into the other of two device output sets."""
     import numpy as np
     import torch
 
@@ -376,25 +379,44 @@ def run_e2e(args, dev, q, code2, x_host, bytes_, world):
     d = dict(packed=torch.empty_like(q.packed), absmax_q=torch.empty_like(q.absmax_q),
              absmax2=torch.empty_like(q.absmax2), code2=torch.empty_like(code2),
              x=torch.empty((1, K_COLS), dtype=torch.bfloat16, device=dev),
-             bf16=torch.empty(n, dtype=torch.bfloat16, device=dev),
-             fp16=torch.empty(n, dtype=torch.float16, device=dev),
              y=torch.empty((1, N_ROWS), dtype=torch.float32, device=dev))
+    outs = [dict(bf16=torch.empty(n, dtype=torch.bfloat16, device=dev),
+                 fp16=torch.empty(n, dtype=torch.float16, device=dev)) for _ in range(2)]
+    main = torch.cuda.current_stream(dev)
+    copy_streams = (torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev))
+    copied = [None, None]   # per output set: events of its last D2H copies
+    count = [0]
     h2d = sum(t.numel() * t.element_size() for t in (h_packed, h_absmax_q, h_absmax2, h_code2, h_x))
     d2h = sum(t.numel() * t.element_size() for t in (h_bf16, h_fp16, h_y))
 
     def step():
+        o = outs[count[0] % 2]
+        slot = count[0] % 2
+        count[0] += 1
         for k, h in (("packed", h_packed), ("absmax_q", h_absmax_q), ("absmax2", h_absmax2),
                      ("code2", h_code2), ("x", h_x)):
             d[k].copy_(h, non_blocking=True)
+        if copied[slot] is not None:   # the copies out of this output set two steps ago are done
+            for e in copied[slot]:
+                main.wait_event(e)
         nf4.nf4_dequant(d["packed"], d["absmax_q"], d["absmax2"], d["code2"], q.offset, n, BS, S2,
-                        out=d["bf16"], out_dtype=torch.bfloat16)
+                        out=o["bf16"], out_dtype=torch.bfloat16)
         nf4.nf4_dequant(d["packed"], d["absmax_q"], d["absmax2"], d["code2"], q.offset, n, BS, S2,
-                        out=d["fp16"], out_dtype=torch.float16)
+                        out=o["fp16"], out_dtype=torch.float16)
         nf4.nf4_gemv(d["packed"], d["absmax_q"], d["absmax2"], d["code2"], q.offset, N_ROWS, K_COLS,
                      d["x"], y=d["y"], blocksize=BS, s2_blocksize=S2)
-        h_bf16.copy_(d["bf16"], non_blocking=True)
-        h_fp16.copy_(d["fp16"], non_blocking=True)
+        done = torch.cuda.Event()
+        done.record(main)
         h_y.copy_(d["y"], non_blocking=True)
+        evs = []
+        for cs, src, dst in ((copy_streams[0], o["bf16"], h_bf16), (copy_streams[1], o["fp16"], h_fp16)):
+            cs.wait_event(done)
+            with torch.cuda.stream(cs):
+                dst.copy_(src, non_blocking=True)
+            e = torch.cuda.Event()
+            e.record(cs)
+            evs.append(e)
+        copied[slot] = evs
 
     steps = max(3, min(args.steps, 50))
     for _ in range(3):
