@@ -137,9 +137,8 @@ NF4_API nf4_status nf4_dequant(const uint8_t* packed, const uint8_t* absmax_q,
  *   x            bfloat16 bit patterns [batch][K], 2-byte aligned.
  *   batch        1 .. 64 activation vectors. 9 .. 64 run on the tensor cores
  *                (one launch) when K is a multiple of 64, blocksize >= 64
- *                and packed and x are 16-byte aligned; otherwise, like
- *                every batch of a shape the fast kernels do not take, in
- *                slabs of up to 8 vectors, one launch each.
+ *                and packed and x are 16-byte aligned, otherwise in slabs
+ *                of up to 8 vectors (one launch each).
  *   y            binary32 [batch][N], 4-byte aligned:
  *                y[b][r] = sum_k W_hat[r][k] * x[b][k], with W_hat[r][k] the
  *                binary32 dequantized weight (before 16-bit rounding) and
