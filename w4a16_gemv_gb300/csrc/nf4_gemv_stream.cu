@@ -733,9 +733,12 @@ cudaError_t launch_b1(const B1Plan& plan, cudaStream_t stream) {
 // (lane-private, 256-byte rows, lane l at byte 8l), so one byte permute, one
 // 64-bit shared load and one packed fma.rn.f32x2 per vector handle a packed
 // byte. The kernel runs BP = 2, 4 or 8 vectors (3 runs as 4, 5..7 as 8 with
-// zero vectors that are not written). Rows longer than the CTA's lanes are
-// walked in column slices; a warp adds its reduced partial of every slice to
-// its own (row, vector) slot, so the sums keep a fixed order.
+// zero vectors that are not written): 16-byte chunks on 512 threads for 2,
+// 8-byte chunks on 512 threads for 4 and on 256 threads for 8 (128 x values
+// per lane). The block scale is applied inside the warp reduction, once a
+// block's lanes are summed. Rows longer than the CTA's lanes are walked in
+// column slices; a warp adds its reduced partial of every slice to its own
+// (row, vector) slot, so the sums keep a fixed order.
 
 template <int BP, int CB>
 struct LaneN {
