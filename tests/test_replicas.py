@@ -1,9 +1,11 @@
-"""The multi-process path of bench.py on the CPU (gloo, world size 2).
+"""The host side of bench.py on the CPU: the multi-process path (gloo, world
+size 2) and the reference arm.
 
 The hot path does not shard across GPUs here: under torch.distributed.run
 every rank runs an independent replica, the job's time is the slowest
 replica's, and the throughput counts every replica's bytes. These tests run
-that host logic with two gloo ranks; no GPU and no CUDA call is involved.
+that host logic with two gloo ranks, and one step of the reference arm (the
+CPU oracle); no GPU and no CUDA call is involved.
 """
 import json
 import os
@@ -70,3 +72,22 @@ def test_reference_arm_prints_only_on_rank_zero():
                        timeout=300)
     assert r.returncode == 0, r.stderr
     assert r.stdout.strip() == ""
+
+
+def test_reference_arm_json_line():
+    """One step of the reference arm (the CPU oracle) on a single process: the
+    JSON line carries the bench's metric, a cpu_baseline describing the run
+    and an e2e entry without host-device copies."""
+    sys.path.insert(0, ROOT)
+    import bench
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "3"], env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stderr
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC
+    assert d["unit"] == "GB/s" and d["higher_is_better"] is True and d["steps"] == 1
+    assert d["value"] > 0 and d["cpu_baseline"]["value"] == d["value"]
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
