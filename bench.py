@@ -680,7 +680,6 @@ def run_sweep(args):
     step of a Qwen2.5-1.5B-shaped decoder at batch 1 and 4. Inputs are
     synthetic random codes and scales (timing does not depend on the values);
     each case rotates over enough input sets to exceed 4x the L2."""
-    import ctypes
     import numpy as np
     import torch
 
