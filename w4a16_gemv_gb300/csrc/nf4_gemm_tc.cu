@@ -585,6 +585,7 @@ cudaError_t try_gemm_tc(const QuantTensor& t, int64_t N, int64_t K, const uint16
                         const YOut& out, int sms, cudaStream_t stream, bool* done) {
   *done = false;
   if (batch < 9 || batch > 64 || N <= 0 || K <= 0 || K % kStageK != 0) return cudaSuccess;
+  if (K > (int64_t(1) << 30)) return cudaSuccess;  // K and stage coordinates stay in 32 bits
   if (t.lbs < 6 || (K & ((int64_t(1) << t.lbs) - 1)) != 0) return cudaSuccess;  // blocksize >= 64, rows whole blocks
   if ((reinterpret_cast<uintptr_t>(t.packed) & 15u) != 0 || (reinterpret_cast<uintptr_t>(x) & 15u) != 0)
     return cudaSuccess;
