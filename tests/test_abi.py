@@ -214,3 +214,20 @@ def test_step_argument_errors(lib):
     assert lib.nf4_step_launch(None, None) == ERR_NULL
     assert lib.nf4_step_destroy(None) == OK
 
+
+
+def test_cuda_failure_is_reported_as_a_status(lib):
+    """Failure detection on the host: on a machine without a usable GPU every
+    CUDA call fails, which stands in for a failing launch. Calls with valid
+    arguments return NF4_ERR_CUDA, record the CUDA error code, and leave the
+    library usable (argument checks still answer). Skipped where a GPU is
+    present: the fake addresses would then reach a kernel."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert dq(lib) == ERR_CUDA
+    assert lib.nf4_last_cuda_error() != 0
+    assert gv(lib) == ERR_CUDA
+    assert lib.nf4_last_cuda_error() != 0
+    assert dq(lib, bs=48) == ERR_BS      # host checks are unaffected
+    assert gv(lib, batch=0) == ERR_BATCH
