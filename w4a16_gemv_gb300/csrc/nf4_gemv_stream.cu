@@ -727,7 +727,7 @@ cudaError_t launch_b1(const B1Plan& plan, cudaStream_t stream) {
 
 // ---------------------------------------------------------------------------
 // Batch 2..8. Same layout as batch 1 (k-stationary, direct weight loads, RPG
-// rows per step, three steps in flight), with x kept in binary32 (bfloat16
+// rows per step, three steps in flight, four on 256 threads), with x kept in binary32 (bfloat16
 // widens exactly, so there is no conversion to check): the lane's x chunk of
 // every vector stays in registers. The code-pair table holds binary32 pairs
 // (lane-private, 256-byte rows, lane l at byte 8l), so one byte permute, one
@@ -854,6 +854,39 @@ __device__ __forceinline__ void consume_n(const uint8_t* lane_src, uint32_t row_
       compute_step_n<BP, CB, RPG>(C, L, sScale, sPart, spr, W, wg, lane, rg0 + (s + 2) * RPG,
                                   rows_of(s + 2), first);
       if (s + 5 < ns) load_step<CB, RPG>(C, src_of(s + 5), row_bytes, rows_of(s + 5));
+    }
+  }
+}
+
+// The same loop with four steps in flight (the 256-thread kernel has the
+// registers for a fourth step buffer).
+template <int BP, int CB, int RPG>
+__device__ __forceinline__ void consume_n4(const uint8_t* lane_src, uint32_t row_bytes,
+                                           Step<CB, RPG>& A, Step<CB, RPG>& B, Step<CB, RPG>& C,
+                                           Step<CB, RPG>& D, const LaneN<BP, CB>& L,
+                                           const float* sScale, float* sPart, int spr, int W, int wg,
+                                           int lane, int rg0, int rg1, bool first) {
+  const int n = rg1 - rg0;
+  const int ns = (n + RPG - 1) / RPG;
+  auto rows_of = [&](int s) { return (n - s * RPG < RPG) ? n - s * RPG : RPG; };
+  auto src_of = [&](int s) { return lane_src + uint32_t(rg0 + s * RPG) * row_bytes; };
+  for (int s = 0; s < ns; s += 4) {
+    compute_step_n<BP, CB, RPG>(A, L, sScale, sPart, spr, W, wg, lane, rg0 + s * RPG, rows_of(s), first);
+    if (s + 4 < ns) load_step<CB, RPG>(A, src_of(s + 4), row_bytes, rows_of(s + 4));
+    if (s + 1 < ns) {
+      compute_step_n<BP, CB, RPG>(B, L, sScale, sPart, spr, W, wg, lane, rg0 + (s + 1) * RPG,
+                                  rows_of(s + 1), first);
+      if (s + 5 < ns) load_step<CB, RPG>(B, src_of(s + 5), row_bytes, rows_of(s + 5));
+    }
+    if (s + 2 < ns) {
+      compute_step_n<BP, CB, RPG>(C, L, sScale, sPart, spr, W, wg, lane, rg0 + (s + 2) * RPG,
+                                  rows_of(s + 2), first);
+      if (s + 6 < ns) load_step<CB, RPG>(C, src_of(s + 6), row_bytes, rows_of(s + 6));
+    }
+    if (s + 3 < ns) {
+      compute_step_n<BP, CB, RPG>(D, L, sScale, sPart, spr, W, wg, lane, rg0 + (s + 3) * RPG,
+                                  rows_of(s + 3), first);
+      if (s + 7 < ns) load_step<CB, RPG>(D, src_of(s + 7), row_bytes, rows_of(s + 7));
     }
   }
 }
@@ -1004,10 +1037,12 @@ __global__ void __launch_bounds__(NT, 1) gemv_bn_kernel(const BNArgs p) {
     const int cc = L.act ? c : p.cpr - 1;
     L.scol = int((int64_t(cc) * CE) >> t.lbs);
     const uint8_t* lane_src = slab + uint32_t(cc) * CB;
-    Step<CB, RPG> A, B, C;
+    Step<CB, RPG> A, B, C, D;
     if (n_steps > 0) load_step<CB, RPG>(A, lane_src + uint32_t(rg0) * rb, rb, rows_of(0));
     if (n_steps > 1) load_step<CB, RPG>(B, lane_src + uint32_t(rg0 + RPG) * rb, rb, rows_of(1));
     if (n_steps > 2) load_step<CB, RPG>(C, lane_src + uint32_t(rg0 + 2 * RPG) * rb, rb, rows_of(2));
+    if (NT == 256 && n_steps > 3)  // a fourth step in flight where the registers allow
+      load_step<CB, RPG>(D, lane_src + uint32_t(rg0 + 3 * RPG) * rb, rb, rows_of(3));
     // x chunk of every vector (bfloat16 -> binary32 exactly); missing
     // vectors and lanes past the row are zero
 #pragma unroll
@@ -1023,8 +1058,12 @@ __global__ void __launch_bounds__(NT, 1) gemv_bn_kernel(const BNArgs p) {
           L.xf[b][4 * q + j] = make_float2(__uint_as_float(w[j] << 16), __uint_as_float(w[j] & 0xffff0000u));
       }
     }
-    consume_n<BP, CB, RPG>(lane_src, rb, A, B, C, L, sScale, sPart, p.spr, p.W, wg, lane, rg0, rg1,
-                           sl == 0);
+    if constexpr (NT == 256)
+      consume_n4<BP, CB, RPG>(lane_src, rb, A, B, C, D, L, sScale, sPart, p.spr, p.W, wg, lane, rg0,
+                              rg1, sl == 0);
+    else
+      consume_n<BP, CB, RPG>(lane_src, rb, A, B, C, L, sScale, sPart, p.spr, p.W, wg, lane, rg0, rg1,
+                             sl == 0);
   }
 
   // End of the group: one sum per (row, vector) over the group's warps.
