@@ -727,9 +727,9 @@ cudaError_t launch_b1(const B1Plan& plan, cudaStream_t stream) {
 
 // ---------------------------------------------------------------------------
 // Batch 2..8. Same layout as batch 1 (k-stationary, direct weight loads, RPG
-// rows per step, three steps in flight, four on 256 threads), with x kept in binary32 (bfloat16
-// widens exactly, so there is no conversion to check): the lane's x chunk of
-// every vector stays in registers. The code-pair table holds binary32 pairs
+// rows per step, three steps in flight, four on 256 threads), with x kept in
+// binary32 (bfloat16 widens exactly, so there is no conversion to check): the
+// lane's x chunk of every vector stays in registers. The code-pair table holds binary32 pairs
 // (lane-private, 256-byte rows, lane l at byte 8l), so one byte permute, one
 // 64-bit shared load and one packed fma.rn.f32x2 per vector handle a packed
 // byte. The kernel runs BP = 2, 4 or 8 vectors (3 runs as 4, 5..7 as 8 with
