@@ -311,7 +311,11 @@ NF4_API nf4_status nf4_quantize(const float* w, int64_t n, int32_t blocksize, in
  *     CUDA call.
  *   Set-up: the first call on each device (with that device current) looks up
  *     the array's device address with cudaGetSymbolAddress and caches it; make
- *     that first call before any stream capture.
+ *     that first call before any stream capture. The cached address belongs
+ *     to the device's primary context as it was then: do not call this entry
+ *     point after cudaDeviceReset on that device, or from a different context
+ *     made current for it (the array would then live at another address).
+ *     nf4_quantize, which takes caller memory, has no such restriction.
  *   Concurrency: the array is shared by all callers on a device, so calls
  *     whose kernels may overlap in time (different streams, or host threads
  *     without an ordering between their streams) race on it; the caller

@@ -69,6 +69,7 @@ def _load():
     lib.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
     lib.oracle_bf16_to_f32.restype = ctypes.c_float
     lib.oracle_code2_linear.argtypes = [P]
+    lib.oracle_code2_dynamic.argtypes = [P]
     lib.oracle_block_absmax.argtypes = [P, I64, I64, P]
     lib.oracle_nf4_nearest.argtypes = [ctypes.c_float]
     lib.oracle_nf4_nearest.restype = ctypes.c_int
@@ -140,6 +141,14 @@ def code2_linear() -> np.ndarray:
     """fp16[256] second-level table, entry i = (i - 127.5) / 127.5 (as uint16 bits)."""
     out = np.zeros(256, np.uint16)
     _load().oracle_code2_linear(_ptr(out))
+    return out
+
+
+def code2_dynamic() -> np.ndarray:
+    """fp16[256] non-linear second-level table: entry 128 + k = 2^((k - 127) / 16),
+    entry 127 - k its negation (as uint16 bits)."""
+    out = np.zeros(256, np.uint16)
+    _load().oracle_code2_dynamic(_ptr(out))
     return out
 
 

@@ -214,6 +214,21 @@ void oracle_code2_linear(uint16_t code2[256]) {
   for (int i = 0; i < 256; ++i) code2[i] = oracle_f64_to_f16(((double)i - 127.5) / 127.5);
 }
 
+/* A non-linear second-level table ("NF4反量化算子优化", section "第二层量化",
+ * stores the scales in an 8-bit floating-point format; this is one such
+ * map): logarithmically spaced magnitudes, sixteen entries per octave.
+ * Entry 128 + k (k = 0..127) is binary16(2^((k - 127) / 16)) and entry
+ * 127 - k its negation, so the table is increasing, antisymmetric and ends
+ * at -1 and +1. The exponent is an exact binary64 quotient; exp2 of it is
+ * rounded once to binary16. */
+void oracle_code2_dynamic(uint16_t code2[256]) {
+  for (int k = 0; k < 128; ++k) {
+    const uint16_t h = oracle_f64_to_f16(exp2(((double)k - 127.0) / 16.0));
+    code2[128 + k] = h;
+    code2[127 - k] = (uint16_t)(h | 0x8000u);
+  }
+}
+
 /* ------------------------------------------------------------------------ */
 /* First-level quantization, [NF4-OPT] "第一层量化" and [NF4-RPT] 1.1:
  * flatten, cut into blocks of `bs` consecutive elements, absmax per block.  */

@@ -95,6 +95,17 @@ def code2_linear() -> np.ndarray:
     return ((np.arange(256, dtype=np.float64) - 127.5) / 127.5).astype(np.float16).view(np.uint16)
 
 
+def code2_dynamic() -> np.ndarray:
+    """A non-linear second-level table for the table-generality cases:
+    logarithmically spaced magnitudes, entry 128 + k = binary16(2^((k - 127) / 16))
+    for k < 128 and entry 127 - k its negation, as uint16 bit patterns."""
+    pos = np.exp2((np.arange(128, dtype=np.float64) - 127.0) / 16.0).astype(np.float16).view(np.uint16)
+    out = np.zeros(256, np.uint16)
+    out[128:] = pos
+    out[:128] = (pos | 0x8000)[::-1]
+    return out
+
+
 # --------------------------------------------------------------------------
 # workloads (shapes, sizes, distributions and seeds of the five configurations)
 

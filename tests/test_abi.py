@@ -231,3 +231,37 @@ def test_cuda_failure_is_reported_as_a_status(lib):
     assert lib.nf4_last_cuda_error() != 0
     assert dq(lib, bs=48) == ERR_BS      # host checks are unaffected
     assert gv(lib, batch=0) == ERR_BATCH
+
+
+def test_calls_from_many_host_threads(lib):
+    """The host side keeps no unsynchronised state: argument checks (and, on
+    a machine without a usable GPU, the CUDA-failure path with its per-thread
+    error record and the per-device caches it passes through) answer the same
+    from eight threads at once as from one."""
+    import threading
+
+    import torch
+    no_gpu = not torch.cuda.is_available()
+    cases = [lambda: gv(lib, batch=0), lambda: gv(lib, K=63), lambda: gv(lib, x=0),
+             lambda: gv(lib, bs=48), lambda: dq(lib, dtype=2), lambda: dq(lib, out=A + 1),
+             lambda: gv(lib, N=0, x=0, y=0)]
+    if no_gpu:
+        cases += [lambda: gv(lib), lambda: dq(lib), lambda: gv(lib, batch=4), lambda: gv(lib, batch=16)]
+    expected = [c() for c in cases]
+    errors = []
+
+    def worker(seed):
+        order = list(range(len(cases))) * 50
+        for i in order[seed::3] + order:
+            got = cases[i]()
+            if got != expected[i]:
+                errors.append((seed, i, got, expected[i]))
+            if no_gpu and got == ERR_CUDA and lib.nf4_last_cuda_error() == 0:
+                errors.append((seed, i, "no CUDA error recorded"))
+
+    threads = [threading.Thread(target=worker, args=(k,)) for k in range(8)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors[:5]

@@ -60,6 +60,23 @@ def test_worked_examples_from_formula(dtype):
         np.testing.assert_array_equal(got, _expected_16bit(v32.astype(np.float64), dtype), err_msg=name)
 
 
+
+def test_worked_example_non_dyadic_scale():
+    """absmax_q 200, absmax2 binary16(0.01), offset binary32(0.03): the scale
+    is not a power-of-two combination, so every binary32 rounding of the
+    formula's steps matters (tests/golden/dequant_nondyadic_example.txt)."""
+    t = _one_block_all_codes(200, _f16(0.01), float(np.float32(0.03)))
+    assert t.absmax2[0] == 0x211F and oracle.code2_linear()[200] == 0x388D
+    bf = oracle.dequant(t, oracle.BF16)
+    hf = oracle.dequant(t, oracle.FP16)
+    # element 2j holds code j % 16 (high nibble of byte j)
+    for idx, e_bf, e_hf in read_golden_rows("dequant_nondyadic_example.txt"):
+        el = 2 * int(idx)
+        assert bf[el] == int(e_bf, 16), (idx, hex(bf[el]))
+        assert hf[el] == int(e_hf, 16), (idx, hex(hf[el]))
+    # the decoded block scale itself, bit for bit
+    assert np.float32(oracle.block_scale(t, 0)).view(np.uint32) == 0x3D122F5A
+
 def test_nibble_order_bytes():
     s = 0.75
     for byte, (e0, e1) in {0x0F: (-s, s), 0xF0: (s, -s), 0x7F: (0.0, s), 0xF7: (s, 0.0)}.items():
@@ -202,13 +219,17 @@ def test_quantize_recovers_exact_codes():
         assert packed[-1] & 15 == 0
 
 
-def _config0_like(n=64 * 256 * 3 + 64 * 5 + 17, seed=11):
+def _config0_like(n=64 * 256 * 3 + 64 * 5 + 17, seed=11, code2=None):
     w = synth.weights(seed, n, 0.001, seed + 1)
-    return w, oracle.quantize(w, 64, 256)
+    if code2 is None:
+        return w, oracle.quantize(w, 64, 256)
+    return w, oracle.quantize(w, 64, 256, code2)
 
 
-def test_quantizer_properties():
-    w, t = _config0_like()
+@pytest.mark.parametrize("table", ["linear", "dynamic"])
+def test_quantizer_properties(table):
+    w, t = _config0_like(code2=None if table == "linear" else oracle.code2_dynamic())
+    assert table == "linear" or np.array_equal(t.code2, oracle.code2_dynamic())
     n = w.size
     bs, s2 = 64, 256
     nb = (n + bs - 1) // bs
@@ -249,6 +270,29 @@ def test_round_trip_bound():
     a2 = t.absmax2.view(np.float16).astype(np.float64)[np.arange(b[-1] + 1) // 256]
     scale_err = np.abs(absmax - s)
     assert np.all(scale_err <= a2 * (1 / 255 + 2.0 ** -11) + 4 * 2.0 ** -24 * np.abs(s))
+    bound = 0.1519036 * absmax[b] + scale_err[b] + 2 * 2.0 ** -24 * np.abs(s[b])
+    assert np.all(np.abs(w.astype(np.float64) - w_hat) <= bound * (1 + 1e-6))
+
+
+def test_round_trip_bound_dynamic_table():
+    """With the non-linear table the second-level error of block b is at most
+    half the gap between the two table entries around r = (absmax - offset) /
+    absmax2, times absmax2 (plus binary32 rounding); the element bound is the
+    same as for the linear table."""
+    w, t = _config0_like(seed=13, code2=oracle.code2_dynamic())
+    n = w.size
+    nb = (n + 63) // 64
+    c2 = oracle.code2_dynamic().view(np.float16).astype(np.float64)
+    absmax = np.array([np.max(np.abs(w[i * 64:(i + 1) * 64])) for i in range(nb)])
+    s = np.array([oracle.block_scale(t, i) for i in range(nb)])
+    a2 = t.absmax2.view(np.float16).astype(np.float64)[np.arange(nb) // 256]
+    r = (absmax - t.offset) / a2
+    j = np.clip(np.searchsorted(c2, r), 1, 255)
+    gap = c2[j] - c2[j - 1]
+    scale_err = np.abs(absmax - s)
+    assert np.all(scale_err <= a2 * (gap / 2 + 2.0 ** -11) + 4 * 2.0 ** -24 * np.abs(s))
+    w_hat = oracle.dequant_f32(t).astype(np.float64)
+    b = np.arange(n) // 64
     bound = 0.1519036 * absmax[b] + scale_err[b] + 2 * 2.0 ** -24 * np.abs(s[b])
     assert np.all(np.abs(w.astype(np.float64) - w_hat) <= bound * (1 + 1e-6))
 

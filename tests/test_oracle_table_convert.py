@@ -143,3 +143,29 @@ def test_code2_linear_table():
 def test_generator_code2_table_matches_oracle():
     import synth
     np.testing.assert_array_equal(synth.code2_linear(), oracle.code2_linear())
+
+
+def test_code2_dynamic_table():
+    """The non-linear second-level table: increasing, antisymmetric, ends at
+    -1/+1, powers of two exactly every sixteenth entry, sixteen entries per
+    octave, consecutive magnitudes in the ratio 2^(1/16) up to binary16
+    rounding."""
+    c = oracle.code2_dynamic()
+    assert c[0] == 0xBC00 and c[255] == 0x3C00
+    np.testing.assert_array_equal(c[::-1], c ^ 0x8000)
+    vals = c.view(np.float16).astype(np.float64)
+    assert np.all(np.diff(vals) > 0)
+    for m in range(8):                      # entry 255 - 16 m is 2^-m, exactly
+        assert c[255 - 16 * m] == (15 - m) << 10, m
+    pos = vals[128:]
+    for m in range(7):                      # 16 entries in each octave [2^-(m+1), 2^-m)
+        assert np.count_nonzero((pos >= 2.0 ** -(m + 1)) & (pos < 2.0 ** -m)) == 16
+    ratio = pos[1:] / pos[:-1]
+    # binary16 carries 11 significant bits: each entry is within 2^-11 relative
+    assert np.all(np.abs(ratio / 2.0 ** (1 / 16) - 1) <= 2 * 2.0 ** -11)
+    assert 2.0 ** -8 < pos[0] < 2.0 ** -7   # smallest magnitude 2^(-127/16)
+
+
+def test_generator_code2_dynamic_matches_oracle():
+    import synth
+    np.testing.assert_array_equal(synth.code2_dynamic(), oracle.code2_dynamic())

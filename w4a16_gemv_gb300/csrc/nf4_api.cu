@@ -7,14 +7,15 @@
 namespace nf4 {
 
 int device_sm_count() {
-  static int cache[64] = {0};
+  static PerDeviceCache cache;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return -1;
-  if (dev < 64 && cache[dev] > 0) return cache[dev];
-  int sms = 0;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
-  if (dev < 64) cache[dev] = sms;
-  return sms;
+  return cache.get(dev, [dev] {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+      return -1;
+    return sms;
+  });
 }
 
 }  // namespace nf4

@@ -29,7 +29,11 @@
 //     idle, a cluster of three CTAs covers a pair of tiles instead.
 // Every wait on an mbarrier is bounded (about one second); a wait that runs
 // out sets bit 0 of the device error flags and the kernel still completes
-// its cluster barriers and frees its tensor memory.
+// its cluster barriers and frees its tensor memory. That path only reports a
+// hang: copies or MMAs that never completed may still be in flight into the
+// CTA's shared or tensor memory when it exits, so after a timeout the
+// launch's results, and the device's state, are undefined. The limit is long
+// enough that only a real hang reaches it.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -537,17 +541,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 // cuTensorMapEncodeTiled from the driver, looked up once.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
+  // initialised once, thread-safely (function-local static)
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void* f = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    tried = true;
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    return PFN_cuTensorMapEncodeTiled_v12000(nullptr);
+  }();
   return fn;
 }
 
@@ -555,15 +558,9 @@ template <int BN>
 cudaError_t launch_tc(const TcArgs& a, const CUtensorMap& tmx, const CUtensorMap& tmw, int grid,
                       uint32_t smem, cudaStream_t stream) {
   auto kern = gemm_tc_kernel<BN>;
-  static int attr_set[64] = {0};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static PerDeviceCache attr_set;
+  const cudaError_t e = set_max_dynamic_smem_once(kern, 227 * 1024, attr_set);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[dev] = 1;
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(grid));
   cfg.blockDim = dim3(unsigned(kTcThreads));

@@ -643,14 +643,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_b1_kernel(const B1Args p) {
 uint32_t align_up_u32(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
 int reserved_smem_per_block() {
-  static int cache[64] = {0};
+  static PerDeviceCache cache;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return -1;
-  if (dev < 64 && cache[dev] > 0) return cache[dev] - 1;  // stored as value + 1
-  int r = 0;
-  if (cudaDeviceGetAttribute(&r, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess) return -1;
-  if (dev < 64) cache[dev] = r + 1;
-  return r;
+  return cache.get(dev, [dev] {
+    int r = 0;
+    if (cudaDeviceGetAttribute(&r, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess) return -1;
+    return r;
+  });
 }
 
 // Shared memory: [code2 | absmax2 | x scales | absmax_q | scales | partial
@@ -710,16 +710,9 @@ bool plan_b1(const SubTensor* subs, int nsub, int64_t K, const uint16_t* x, int 
 template <int CB, int NT, int NSUB>
 cudaError_t launch_b1(const B1Plan& plan, cudaStream_t stream) {
   auto kern = gemv_b1_kernel<CB, NF4_B1_RPG, NT, NSUB>;
-  static int attr_set[64] = {0};
-  int dev = 0;
-  const cudaError_t ed = cudaGetDevice(&dev);
-  if (ed != cudaSuccess) return ed;
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmemPerCta);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[dev] = 1;
-  }
+  static PerDeviceCache attr_set;
+  const cudaError_t e = set_max_dynamic_smem_once(kern, kMaxSmemPerCta, attr_set);
+  if (e != cudaSuccess) return e;
   return launch_k(kern, dim3(unsigned(plan.grid)), dim3(unsigned(NT)), plan.smem_bytes, stream,
                   plan.a);
 }
@@ -1135,25 +1128,11 @@ bool plan_bn(const SubTensor* subs, int nsub, int64_t K, const uint16_t* x, int 
   return *smem_bytes <= uint32_t(kMaxSmemPerCta);
 }
 
-template <typename Kern>
-cudaError_t set_smem_limit_once(Kern kern, int* attr_set) {
-  int dev = 0;
-  const cudaError_t ed = cudaGetDevice(&dev);
-  if (ed != cudaSuccess) return ed;
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmemPerCta);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[dev] = 1;
-  }
-  return cudaSuccess;
-}
-
 template <int BP, int CB, int NSUB, int NT>
 cudaError_t launch_bn(const BNArgs& a, int grid, uint32_t smem_bytes, cudaStream_t stream) {
   auto kern = gemv_bn_kernel<BP, CB, 2, NSUB, NT>;
-  static int attr_set[64] = {0};
-  const cudaError_t e = set_smem_limit_once(kern, attr_set);
+  static PerDeviceCache attr_set;
+  const cudaError_t e = set_max_dynamic_smem_once(kern, kMaxSmemPerCta, attr_set);
   if (e != cudaSuccess) return e;
   return launch_k(kern, dim3(unsigned(grid)), dim3(unsigned(NT)), smem_bytes, stream, a);
 }

@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <utility>
 
 #include "nf4.h"
@@ -108,6 +109,46 @@ __device__ __forceinline__ uint4 ldg_stream_u128(const void* p) {
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p));
   return v;
+}
+
+// Per-device values that the host side looks up once (device attributes, a
+// kernel attribute already set) and then reads from any host thread. Each
+// slot is an atomic: concurrent first calls may each run the (idempotent)
+// lookup and store the same value; later calls read it without a lock.
+constexpr int kMaxCachedDevices = 64;
+class PerDeviceCache {
+ public:
+  // The stored value for `dev`, else compute(): a result >= 0 is stored, a
+  // negative one (an error) is returned and not stored. Devices beyond the
+  // cache always compute.
+  template <typename F>
+  int get(int dev, F&& compute) {
+    const bool cached = dev >= 0 && dev < kMaxCachedDevices;
+    if (cached) {
+      const int v = slot_[dev].load(std::memory_order_acquire);
+      if (v > 0) return v - 1;
+    }
+    const int r = compute();
+    if (cached && r >= 0) slot_[dev].store(r + 1, std::memory_order_release);
+    return r;
+  }
+
+ private:
+  std::atomic<int> slot_[kMaxCachedDevices] = {};  // value + 1; 0: not yet known
+};
+
+// Raises `kern`'s dynamic shared memory limit to `bytes` once per device.
+template <typename Kern>
+cudaError_t set_max_dynamic_smem_once(Kern kern, int bytes, PerDeviceCache& done) {
+  int dev = 0;
+  const cudaError_t ed = cudaGetDevice(&dev);
+  if (ed != cudaSuccess) return ed;
+  cudaError_t err = cudaSuccess;
+  done.get(dev, [&] {
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    return err == cudaSuccess ? 1 : -1;
+  });
+  return err;
 }
 
 // Per-device properties cached on first use (SM count).
