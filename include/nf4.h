@@ -89,8 +89,9 @@ NF4_API int nf4_last_cuda_error(void);
  * nf4_device_error_flags -- read and clear the library's device-side error
  * flags. Bit 0 is set when a bounded wait of the tensor-core GEMV (batches
  * 9..64) on its own copy or MMA pipeline ran out (about one second); that
- * launch then writes NaN or incomplete values to its outputs and finishes
- * instead of hanging. Synchronises with the device (cudaMemcpyFromSymbol).
+ * launch then writes undefined values to its outputs and finishes instead
+ * of hanging. The flags are one word per device, shared by every stream and
+ * caller of the library. Synchronises with the device (cudaMemcpyFromSymbol).
  * `flags` is a host pointer.
  * Errors: NF4_ERR_NULL, NF4_ERR_CUDA.
  */

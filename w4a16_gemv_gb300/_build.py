@@ -12,8 +12,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libnf4.so")
-SOURCES = ("nf4_api.cu", "nf4_dequant.cu", "nf4_gemv.cu", "nf4_gemv_stream.cu", "nf4_quantize.cu",
-           "nf4_step.cu", "nf4_gemm_tc.cu")
+SOURCES = ("nf4_api.cu", "nf4_dequant.cu", "nf4_gemv.cu", "nf4_gemv_b1.cu", "nf4_gemv_stream.cu",
+           "nf4_quantize.cu", "nf4_step.cu", "nf4_gemm_tc.cu")
 GENCODE = "arch=compute_103a,code=sm_103a"
 
 

@@ -1,0 +1,252 @@
+// nf4_gemv_common.cuh -- pieces shared by the streaming GEMV kernels
+// (batch 1 and batches 2..8): grouped-launch planning, ordered small loads,
+// warp reductions, register step buffers and shared-memory helpers.
+#pragma once
+
+#include "nf4_internal.cuh"
+
+namespace nf4 {
+namespace {
+
+constexpr int kMaxGroups = 15;         // named barriers 1..15
+
+// The weight CTA `cta` serves, selected with compile-time indices only (no
+// dynamic indexing of the parameter block).
+template <int NSUB>
+__device__ __forceinline__ SubTensor pick_sub(const SubTensor (&s)[kMaxSub], int nsub, int cta) {
+  SubTensor v = s[0];
+#pragma unroll
+  for (int i = 1; i < NSUB; ++i)
+    if (i < nsub && cta >= s[i].cta0) v = s[i];
+  return v;
+}
+constexpr uint32_t kTabBytes = 65536;  // 256 rows of 256 B
+constexpr int kMaxSmemPerCta = 227 * 1024;
+
+// Everything a launch needs, in one argument block. A launch serves one to
+// kMaxSub weights that share x (a grouped launch): CTAs [cta0, cta0 + ctas)
+
+bool any_bias(const SubTensor* subs, int nsub) {
+  for (int j = 0; j < nsub; ++j)
+    if (subs[j].out.bias) return true;
+  return false;
+}
+
+// Spreads one wave of CTAs (at most `sms`) over the weights of a launch in
+// proportion to their rows, at least one CTA per weight and at most one per
+// row, and fills cta0 / ctas of out[]. Returns the largest number of rows a
+// CTA owns, or -1 when the weights cannot share a launch (an empty weight,
+// or block sizes that differ).
+int assign_ctas(const SubTensor* subs, int nsub, int sms, SubTensor* out, int* grid_out) {
+  if (nsub < 1 || nsub > kMaxSub || sms < nsub) return -1;
+  int64_t total = 0;
+  for (int j = 0; j < nsub; ++j) {
+    if (subs[j].N <= 0 || subs[j].t.lbs != subs[0].t.lbs || subs[j].t.ls2 != subs[0].t.ls2)
+      return -1;
+    total += subs[j].N;
+  }
+  const int grid = int(total < sms ? total : sms);
+  int ctas[kMaxSub];
+  int used = 0;
+  for (int j = 0; j < nsub; ++j) {
+    int64_t c = int64_t(grid) * subs[j].N / total;
+    if (c < 1) c = 1;
+    if (c > subs[j].N) c = subs[j].N;
+    ctas[j] = int(c);
+    used += ctas[j];
+  }
+  // rows per CTA of weight j with c CTAs, rounded up
+  auto load = [&](int j, int c) { return (subs[j].N + c - 1) / c; };
+  while (used < grid) {  // give the spare CTAs to the most loaded weights
+    int best = -1;
+    for (int j = 0; j < nsub; ++j)
+      if (ctas[j] < subs[j].N && (best < 0 || load(j, ctas[j]) > load(best, ctas[best]))) best = j;
+    if (best < 0) break;
+    ++ctas[best];
+    ++used;
+  }
+  while (used > grid) {  // take back from the least loaded
+    int best = -1;
+    for (int j = 0; j < nsub; ++j)
+      if (ctas[j] > 1 && (best < 0 || load(j, ctas[j] - 1) < load(best, ctas[best] - 1))) best = j;
+    if (best < 0) return -1;
+    --ctas[best];
+    --used;
+  }
+  int64_t max_rows = 0;
+  int c0 = 0;
+  for (int j = 0; j < kMaxSub; ++j) {
+    if (j < nsub) {
+      out[j] = subs[j];
+      out[j].cta0 = c0;
+      out[j].ctas = ctas[j];
+      c0 += ctas[j];
+      const int64_t r = load(j, ctas[j]);
+      if (r > max_rows) max_rows = r;
+    } else {
+      out[j] = out[0];
+      out[j].cta0 = used;  // never selected: past the last CTA
+    }
+  }
+  *grid_out = used;
+  return max_rows > (int64_t(1) << 30) ? -1 : int(max_rows);
+}
+
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint4 lds_u128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+// Prologue loads as volatile PTX, so that they are issued in program order
+// (ahead of the weight stream) instead of being moved to their first use.
+__device__ __forceinline__ uint4 ldg_v4_ordered(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint16_t ldg_u16_ordered(const uint16_t* p) {
+  unsigned short v;
+  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ldg_u32_ordered(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+// Bias bits of row r (16 or 32 bits as stored), issued in program order.
+__device__ __forceinline__ uint32_t bias_bits_ordered(const YOut& o, int64_t r) {
+  if (o.dtype == NF4_F32) return ldg_u32_ordered(reinterpret_cast<const uint32_t*>(o.bias) + r);
+  return ldg_u16_ordered(reinterpret_cast<const uint16_t*>(o.bias) + r);
+}
+__device__ __forceinline__ uint8_t ldg_u8_ordered(const uint8_t* p) {
+  unsigned int v;
+  asm volatile("ld.global.nc.u8 %0, [%1];" : "=r"(v) : "l"(p));
+  return uint8_t(v);
+}
+
+__device__ __forceinline__ void named_barrier(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// acc_a += T(low half) * x(low half), acc_b += T(high half) * x(high half):
+// binary16 inputs (code pair and x pair, each packed in 32 bits), binary32
+// accumulation (the products are exact).
+__device__ __forceinline__ void fma2_f16_f32(uint32_t tpair, uint32_t xpair, float& acc_a,
+                                             float& acc_b) {
+  asm("{\n\t.reg .f16 t0, t1, x0, x1;\n\t"
+      "mov.b32 {t0, t1}, %2;\n\t"
+      "mov.b32 {x0, x1}, %3;\n\t"
+      "fma.rn.f32.f16 %0, t0, x0, %0;\n\t"
+      "fma.rn.f32.f16 %1, t1, x1, %1;\n\t}"
+      : "+f"(acc_a), "+f"(acc_b)
+      : "r"(tpair), "r"(xpair));
+}
+
+__device__ __forceinline__ float2 half2_bits_to_float2(uint32_t h) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+
+// Sum V values over the 32 lanes of a warp. On return lane l holds the total
+// of value index transposed_index<V>(l); lanes l < V cover every index once.
+template <int V>
+__device__ __forceinline__ float transposed_warp_reduce(float (&v)[V], int lane) {
+#pragma unroll
+  for (int step = 0; (1 << step) < V; ++step) {
+    const int cnt = V >> step;
+    const int m = 1 << step;
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int i = 0; i < cnt / 2; ++i) {
+      const float send = upper ? v[i] : v[i + cnt / 2];
+      const float keep = upper ? v[i + cnt / 2] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+    }
+  }
+  float r = v[0];
+#pragma unroll
+  for (int m = V; m < 32; m <<= 1) r += __shfl_xor_sync(0xffffffffu, r, m);
+  return r;
+}
+
+template <int V>
+__device__ __forceinline__ int transposed_index(int lane) {
+  int r = 0;
+#pragma unroll
+  for (int step = 0; (1 << step) < V; ++step)
+    if (lane & (1 << step)) r += V >> (step + 1);
+  return r;
+}
+
+// First row (relative to the CTA) of row group g: balanced contiguous split.
+__device__ __forceinline__ int group_row0(int nrows, int G, int g) {
+  const int q = nrows / G, r = nrows - q * G;
+  return q * g + (g < r ? g : r);
+}
+
+// Shared offset of the binary16 x chunk c: the upper 128 bytes of table rows,
+// 32 / CB chunks of 4 * CB bytes per row.
+template <int CB>
+__device__ __forceinline__ uint32_t x16_offset(int c) {
+  constexpr int per_row = 32 / CB;
+  return uint32_t(c / per_row) * 256u + 128u + uint32_t(c % per_row) * uint32_t(4 * CB);
+}
+
+// One step of RPG rows of this lane's column chunk, held in registers.
+template <int CB, int RPG>
+struct Step {
+  uint32_t w[RPG][CB / 4];
+};
+
+template <int CB, int RPG>
+__device__ __forceinline__ void load_step(Step<CB, RPG>& st, const uint8_t* p, uint32_t row_bytes,
+                                          int rows) {
+#pragma unroll
+  for (int r = 0; r < RPG; ++r) {
+    if (r < rows) {
+      if constexpr (CB == 16) {
+        const uint4 v = ldg_stream_u128(p + r * row_bytes);
+        st.w[r][0] = v.x; st.w[r][1] = v.y; st.w[r][2] = v.z; st.w[r][3] = v.w;
+      } else if constexpr (CB == 4) {
+        st.w[r][0] = ldg_stream_u32(p + r * row_bytes);
+      } else {
+        uint2 v;
+        asm volatile("ld.global.nc.L1::no_allocate.v2.b32 {%0,%1}, [%2];"
+                     : "=r"(v.x), "=r"(v.y)
+                     : "l"(p + r * row_bytes));
+        st.w[r][0] = v.x; st.w[r][1] = v.y;
+      }
+    }
+  }
+}
+
+// Dot product of one row's chunk (CB packed bytes in w) with the lane's x
+// chunk. kFast: binary16 x (pre-scaled) and mixed-precision FMAs on the
+// binary16 code pairs; otherwise binary32 x and packed binary32 FMAs.
+uint32_t align_up_u32(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
+
+int reserved_smem_per_block() {
+  static PerDeviceCache cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return -1;
+  return cache.get(dev, [dev] {
+    int r = 0;
+    if (cudaDeviceGetAttribute(&r, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess) return -1;
+    return r;
+  });
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace nf4
