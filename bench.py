@@ -334,6 +334,17 @@ def run_native(args, rank, world, local_rank):
             "weight_bytes": st["weight_bytes"], "gbs": round(gbs, 1),
             "frac_of_measured_hbm": round(gbs / peak, 4)}
         st["close"]()
+    if rank == 0 and world == 1 and not args.no_layers:
+        # every GEMV layer shape of the configurations, timed on its own
+        # (after the timed region; graphs of back-to-back launches over > 4x L2)
+        layers = gemv_layer_times(dev, GEMV_LAYER_CASES, peak)
+        result["detail"]["gemv_layers"] = layers
+        gate = [d for d in layers if d["case"].startswith("llama-7b") and d["batch"] == 1]
+        result["gemv_gate"] = {
+            "target": "batch-1 fused GEMV >= 60% of measured HBM on the 4096x4096 and 7B-shaped layers",
+            "layers": {f"{d['N']}x{d['K']}": {"us_per_layer": d["us_per_layer"], "gbs": d["gbs"],
+                                              "frac_of_measured_hbm": d["frac_of_measured_hbm"]} for d in gate},
+            "peak": peak, "peak_source": peak_src}
     if rank == 0 and world == 1 and not args.no_cpu:
         result["cpu_baseline"] = cpu_baseline(args, q, x_host, bytes_)
     return result
@@ -553,6 +564,63 @@ def _sweep_time(launch, nsets, reps=5):
     return best
 
 
+# The GEMV layer shapes of the configurations: the Qwen2.5-1.5B-shaped layers
+# at batch 1 and the Llama-7B-shaped layers at batches 1, 4 and 8.
+GEMV_LAYER_CASES = ([("qwen q/o", 1536, 1536, 1), ("qwen k/v", 256, 1536, 1), ("qwen gate/up", 8960, 1536, 1),
+                     ("qwen down", 1536, 8960, 1)] +
+                    [(f"llama-7b {nm}", N, K, b) for nm, N, K in
+                     (("attn", 4096, 4096), ("gate/up", 11008, 4096), ("down", 4096, 11008)) for b in (1, 4, 8)])
+
+
+def gemv_layer_times(dev, cases, peak, gen=None, l2=None):
+    """us per layer of nf4_gemv for each (name, N, K, batch): a CUDA graph of
+    back-to-back launches rotating over enough input sets (random codes and
+    scales, x ~ N(0,1) bf16, fp32 y) to exceed 4x the L2, best of 5 replays.
+    Bytes: packed + absmax_q + absmax2 + code2 + x + y."""
+    import numpy as np
+    import torch
+
+    import w4a16_gemv_gb300 as nf4
+    lib = nf4._lib
+    if gen is None:
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(2468)
+    if l2 is None:
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    code2 = torch.from_numpy((((np.arange(256) - 127.5) / 127.5).astype(np.float16))).to(dev)
+    out = []
+    for name, N, K, batch in cases:
+        n = N * K
+        nb = (n + BS - 1) // BS
+        ng = (nb + S2 - 1) // S2
+        bytes_ = n // 2 + nb + 2 * ng + 512 + 2 * batch * K + 4 * batch * N
+        r = max(2, int(math.ceil(4 * l2 / bytes_)))
+        sets = []
+        for _ in range(r):
+            sets.append(dict(packed=torch.randint(0, 256, (n // 2,), dtype=torch.uint8, device=dev, generator=gen),
+                             absmax_q=torch.randint(0, 256, (nb,), dtype=torch.uint8, device=dev, generator=gen),
+                             absmax2=(torch.rand(ng, device=dev, generator=gen) * 0.04 + 0.01).half(),
+                             x=torch.randn(batch, K, device=dev, generator=gen).to(torch.bfloat16),
+                             y=torch.empty(batch, N, device=dev)))
+
+        def launch(i, sp, N=N, K=K, batch=batch, sets=sets):
+            st = sets[i]
+            rc = lib.nf4_gemv(st["packed"].data_ptr(), st["absmax_q"].data_ptr(), st["absmax2"].data_ptr(),
+                              code2.data_ptr(), 0.01, N, K, BS, S2, st["x"].data_ptr(), batch,
+                              st["y"].data_ptr(), sp)
+            if rc != 0:
+                raise RuntimeError(f"nf4_gemv: {nf4.nf4_status_string(rc)}")
+        us = _sweep_time(launch, r)
+        gbs = bytes_ / us / 1e3
+        out.append({"case": name, "N": N, "K": K, "batch": batch, "bytes": bytes_,
+                    "us_per_layer": round(us, 3), "gbs": round(gbs, 1),
+                    "frac_of_measured_hbm": round(gbs / peak, 4), "frac_of_8000": round(gbs / 8000.0, 4),
+                    "sets": r})
+        del sets
+        torch.cuda.empty_cache()
+    return out
+
+
 # Linear layers of one decoder layer: (N, K) of q, k, v, o, gate, up, down.
 DECODERS = {
     "qwen2.5-1.5b": dict(layers=28, hidden=1536, qkv_bias=True,
@@ -648,6 +716,31 @@ def run_one_gemv(args):
     return {"gemv": [N, K, B], "launches": args.steps, "mean_abs_y": float(y.abs().mean())}
 
 
+def run_one_dequant(args):
+    """--dequant N: --steps launches of nf4_dequant of N elements (bf16 out) on
+    random codes and scales (a fixed, small command line to put under a
+    profiler; N = 234881024 is the 28672x8192 case, larger than L2)."""
+    import numpy as np
+    import torch
+
+    import w4a16_gemv_gb300 as nf4
+    n = int(args.dequant)
+    dev = torch.device("cuda:0")
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(778)
+    code2 = torch.from_numpy((((np.arange(256) - 127.5) / 127.5).astype(np.float16))).to(dev)
+    nb = (n + BS - 1) // BS
+    packed = torch.randint(0, 256, ((n + 1) // 2,), dtype=torch.uint8, device=dev, generator=gen)
+    aq = torch.randint(0, 256, (nb,), dtype=torch.uint8, device=dev, generator=gen)
+    a2 = (torch.rand((nb + S2 - 1) // S2, device=dev, generator=gen) * 0.04 + 0.01).half()
+    out = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    for _ in range(args.steps):
+        nf4.nf4_dequant(packed, aq, a2, code2, 0.001, n, BS, S2, out=out, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    return {"dequant": n, "launches": args.steps, "bytes_per_launch": (n + 1) // 2 + nb + 2 * ((nb + S2 - 1) // S2)
+            + 512 + 2 * n}
+
+
 def run_decode_step(args):
     """--decode-step: W replays untimed, then K replays back to back between
     two events; one JSON line."""
@@ -738,38 +831,9 @@ def run_sweep(args):
         del sets
         torch.cuda.empty_cache()
 
-    gv_cases = [("cfg2 q/o", 1536, 1536), ("cfg2 k/v", 256, 1536), ("cfg2 gate/up", 8960, 1536),
-                ("cfg2 down", 1536, 8960), ("cfg3 attn", 4096, 4096), ("cfg3 gate/up", 11008, 4096),
-                ("cfg3 down", 4096, 11008)]
-    for name, N, K in gv_cases:
-        for batch in ((1,) if name.startswith("cfg2") else (1, 4, 8)):
-            n = N * K
-            nb = (n + BS - 1) // BS
-            ng = (nb + S2 - 1) // S2
-            bytes_ = n // 2 + nb + 2 * ng + 512 + 2 * batch * K + 4 * batch * N
-            r = max(2, nsets_for(bytes_))
-            sets = []
-            for _ in range(r):
-                st = quant_set(n)
-                st["x"] = torch.randn(batch, K, device=dev, generator=gen).to(torch.bfloat16)
-                st["y"] = torch.empty(batch, N, device=dev)
-                sets.append(st)
-
-            def launch(i, sp, N=N, K=K, batch=batch, sets=sets):
-                st = sets[i]
-                rc = lib.nf4_gemv(st["packed"].data_ptr(), st["absmax_q"].data_ptr(), st["absmax2"].data_ptr(),
-                                  code2.data_ptr(), 0.01, N, K, BS, S2, st["x"].data_ptr(), batch,
-                                  st["y"].data_ptr(), sp)
-                if rc != 0:
-                    raise RuntimeError(f"nf4_gemv: {nf4.nf4_status_string(rc)}")
-            us = _sweep_time(launch, r)
-            gbs = bytes_ / us / 1e3
-            out.append({"kind": "gemv", "case": name, "N": N, "K": K, "batch": batch, "bytes": bytes_,
-                        "us_per_layer": round(us, 3), "gbs": round(gbs, 1),
-                        "frac_of_measured_hbm": round(gbs / peak, 4), "frac_of_8000": round(gbs / 8000.0, 4),
-                        "sets": r})
-            del sets
-            torch.cuda.empty_cache()
+    for d in gemv_layer_times(dev, GEMV_LAYER_CASES, peak, gen, l2):
+        d["kind"] = "gemv"
+        out.append(d)
     # Output stage fused (bf16 y + bias) and batches above 8 (slabs of eight).
     ex_cases = [("cfg2 q/o bf16+bias", 1536, 1536, 1), ("cfg2 k/v bf16+bias", 256, 1536, 1),
                 ("cfg3 attn bf16+bias", 4096, 4096, 1)]
@@ -854,6 +918,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-step", action="store_true", help="skip the decode-step detail")
+    ap.add_argument("--no-layers", action="store_true", help="skip the per-layer GEMV detail")
     ap.add_argument("--sweep", action="store_true",
                     help="time every dequant and GEMV configuration instead of the step")
     ap.add_argument("--decode-step", action="store_true",
@@ -861,6 +926,8 @@ def main():
     ap.add_argument("--batch", type=int, default=1, help="batch of --decode-step")
     ap.add_argument("--model", choices=sorted(DECODERS), default="qwen2.5-1.5b",
                     help="decoder shape of --decode-step")
+    ap.add_argument("--dequant", type=int, default=None, metavar="N",
+                    help="--steps launches of one bf16 dequant of N elements (for profilers)")
     ap.add_argument("--gemv", type=str, default=None, metavar="N,K,B",
                     help="run --steps launches of one N x K fused GEMV at batch B (for profilers)")
     args = ap.parse_args()
@@ -887,6 +954,10 @@ def main():
     if args.gemv:
         if rank == 0:
             print(json.dumps(run_one_gemv(args)), flush=True)
+        return
+    if args.dequant:
+        if rank == 0:
+            print(json.dumps(run_one_dequant(args)), flush=True)
         return
 
     if world > 1:
