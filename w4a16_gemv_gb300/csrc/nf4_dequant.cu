@@ -226,17 +226,26 @@ __global__ void __launch_bounds__(kThreads) dequant_generic_kernel(QuantTensor t
                               int64_t(gridDim.x) * blockDim.x, out);
 }
 
-#ifndef NF4_DQ_UNROLL
-#define NF4_DQ_UNROLL 2
-#endif
 #ifndef NF4_DQ_BLOCKS_PER_SM
 #define NF4_DQ_BLOCKS_PER_SM 4
 #endif
 #ifndef NF4_DQ_PDL
 #define NF4_DQ_PDL 0
 #endif
-constexpr int kUnroll = NF4_DQ_UNROLL;           // tiles per warp per pipeline step
 constexpr int kBlocksPerSm = NF4_DQ_BLOCKS_PER_SM;  // persistent CTAs per SM
+
+template <bool kBF16, int U>
+cudaError_t launch_tiles(const QuantTensor& t, int64_t n, int64_t ntiles, uint16_t* out, int sms,
+                         cudaStream_t stream) {
+  int64_t blocks = (ntiles + int64_t(kWarps) * U - 1) / (int64_t(kWarps) * U);
+  if (blocks < 1) blocks = 1;
+  if (blocks > int64_t(sms) * kBlocksPerSm) blocks = int64_t(sms) * kBlocksPerSm;
+  if (t.lbs >= 6)
+    return launch_k_pdl(NF4_DQ_PDL, dequant_tiles_kernel<kBF16, U, true>, dim3(unsigned(blocks)),
+                        dim3(kThreads), 0, stream, t, n, ntiles, out);
+  return launch_k_pdl(NF4_DQ_PDL, dequant_tiles_kernel<kBF16, U, false>, dim3(unsigned(blocks)),
+                      dim3(kThreads), 0, stream, t, n, ntiles, out);
+}
 
 template <bool kBF16>
 cudaError_t launch_typed(const QuantTensor& t, int64_t n, uint16_t* out, cudaStream_t stream) {
@@ -245,15 +254,14 @@ cudaError_t launch_typed(const QuantTensor& t, int64_t n, uint16_t* out, cudaStr
   const bool vec_ok = t.lbs >= 3 && (reinterpret_cast<uintptr_t>(t.packed) & 3u) == 0 &&
                       (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
   if (vec_ok) {
+    // Tiles per warp step by size (measured on GB300): one when the tensor
+    // gives the warps under two tiles each (1024^2: 3.0 -> 2.7 us), four from
+    // 32 tiles per warp (28672x8192: 101 -> 94 us), two in between.
     const int64_t ntiles = n / kTileElems;
-    int64_t blocks = (ntiles + int64_t(kWarps) * kUnroll - 1) / (int64_t(kWarps) * kUnroll);
-    if (blocks < 1) blocks = 1;
-    if (blocks > int64_t(sms) * kBlocksPerSm) blocks = int64_t(sms) * kBlocksPerSm;
-    if (t.lbs >= 6)
-      return launch_k_pdl(NF4_DQ_PDL, dequant_tiles_kernel<kBF16, kUnroll, true>,
-                          dim3(unsigned(blocks)), dim3(kThreads), 0, stream, t, n, ntiles, out);
-    return launch_k_pdl(NF4_DQ_PDL, dequant_tiles_kernel<kBF16, kUnroll, false>,
-                        dim3(unsigned(blocks)), dim3(kThreads), 0, stream, t, n, ntiles, out);
+    const int64_t warps = int64_t(sms) * kBlocksPerSm * kWarps;
+    if (ntiles < 2 * warps) return launch_tiles<kBF16, 1>(t, n, ntiles, out, sms, stream);
+    if (ntiles >= 32 * warps) return launch_tiles<kBF16, 4>(t, n, ntiles, out, sms, stream);
+    return launch_tiles<kBF16, 2>(t, n, ntiles, out, sms, stream);
   } else {
     const int64_t nbytes = (n + 1) / 2;
     int64_t blocks = (nbytes + kThreads - 1) / kThreads;
