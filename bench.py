@@ -687,7 +687,7 @@ def decode_step(dev, gen, code2, batch, model="qwen2.5-1.5b"):
             us = e0.elapsed_time(e1) * 1e3 / m
             best = us if best is None else min(best, us)
         return best
-    return {"time": time_step, "weight_bytes": wbytes, "launches": 4 * layers, "linears": 7 * layers,
+    return {"time": time_step, "weight_bytes": wbytes, "launches": step.kernel_count(), "linears": 7 * layers,
             "close": step.close}
 
 

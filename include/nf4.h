@@ -251,6 +251,16 @@ NF4_API nf4_status nf4_step_launch(nf4_step_t step, nf4_stream_t stream);
 NF4_API nf4_status nf4_step_destroy(nf4_step_t step);
 
 /*
+ * nf4_step_kernel_count -- number of kernel launches one replay of `step`
+ * performs (the kernel nodes of its recorded graph), to check how nodes were
+ * grouped: the per-call fixed cost that "RTX 4060 上的 LLM 量化实测", section
+ * "为什么是 k/v projection", finds dominating thin layers is paid once per
+ * launch. `count` is a host pointer; 0 for a step whose nodes were all empty.
+ * Errors: NF4_ERR_NULL, NF4_ERR_CUDA.
+ */
+NF4_API nf4_status nf4_step_kernel_count(nf4_step_t step, int32_t* count);
+
+/*
  * nf4_quantize_workspace_size -- bytes of device workspace nf4_quantize needs
  * for n elements (0 for n <= 0 or unsupported block sizes).
  */

@@ -31,7 +31,7 @@ def test_exports_every_declared_symbol(lib):
     assert set(names) == {"nf4_version", "nf4_status_string", "nf4_last_cuda_error", "nf4_dequant",
                           "nf4_gemv", "nf4_gemv_ex", "nf4_quantize_workspace_size", "nf4_quantize",
                           "nf4_device_error_flags", "nf4_quantize_noalloc", "nf4_step_create",
-                          "nf4_step_launch", "nf4_step_destroy"}
+                          "nf4_step_launch", "nf4_step_destroy", "nf4_step_kernel_count"}
     for n in names:
         assert hasattr(lib, n), n
 
@@ -213,6 +213,7 @@ def test_step_argument_errors(lib):
     assert create([node(K=63)]) == ERR_SIZE
     assert lib.nf4_step_launch(None, None) == ERR_NULL
     assert lib.nf4_step_destroy(None) == OK
+    assert lib.nf4_step_kernel_count(None, None) == ERR_NULL
 
 
 

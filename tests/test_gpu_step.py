@@ -39,7 +39,7 @@ def _round_all(v: np.ndarray, dtype: int) -> np.ndarray:
     return np.vectorize(lambda a: oracle.round_f64(a, dtype), otypes=[np.uint32])(v)
 
 
-def _check_dag(spec, batch, seed):
+def _check_dag(spec, batch, seed, kernels=None):
     """spec: list of (N, K, y dtype, has_bias, input) nodes. Builds the step
     from oracle-quantized weights, runs it once and checks every node's
     output against the oracle with the carried error bound:
@@ -63,6 +63,8 @@ def _check_dag(spec, batch, seed):
     x_bits = synth.activations(seed + 99, batch, spec[0][1])
     x = u16_to_torch(x_bits, torch.bfloat16).view(batch, -1)
     step = nf4.DecodeStep(nodes, x)
+    if kernels is not None:
+        assert step.kernel_count() == kernels
     step.launch()
     torch.cuda.synchronize()
     assert nf4.nf4_device_error_flags() == 0
@@ -115,7 +117,49 @@ def _small_decoder(layers, h=512, kv=128, inter=1536):
 def test_decoder_graph_parity(batch):
     """Two decoder layers: eight launches (q/k/v and gate/up grouped) up to
     batch 8; one tensor-core launch per node at batch 16."""
-    _check_dag(_small_decoder(2), batch, 260)
+    _check_dag(_small_decoder(2), batch, 260, kernels=8 if batch <= 8 else 14)
+
+
+@pytest.mark.parametrize("batch", [1, 4])
+def test_large_group_with_small_arrays_above_the_table(batch):
+    """gate/up-sized pair sharing one launch: at batch 4 the per-CTA scales,
+    absmax_q and partial sums (145 rows x 64 blocks) no longer fit below the
+    pair table and are placed above it; parity against the oracle."""
+    spec = [(11008, 4096, BF16, False, -1), (11008, 4096, BF16, False, -1)]
+    _check_dag(spec, batch, 330, kernels=1)
+
+
+@pytest.mark.parametrize("model", ["qwen", "llama"])
+def test_full_size_layers_group_qkv_and_gate_up(model):
+    """At the Qwen2.5-1.5B and Llama-7B layer shapes (random codes and
+    scales; grouping only, no parity), k and v share q's launch and up shares
+    gate's: four launches per decoder layer at batch 1 and batch 4."""
+    import w4a16_gemv_gb300 as nf4
+    h, kv, inter = (1536, 256, 8960) if model == "qwen" else (4096, 4096, 11008)
+    g = torch.Generator(device=dev())
+    g.manual_seed(31)
+    code2 = u16_to_torch(synth.code2_linear(), torch.float16)
+    for batch in (1, 4):
+        nodes = []
+        for layer in range(2):
+            base = 7 * layer
+            inp = -1 if layer == 0 else base - 1
+            for j, (N, K, src) in enumerate([(h, h, inp), (kv, h, inp), (kv, h, inp), (h, h, base),
+                                             (inter, h, base + 3), (inter, h, base + 3), (h, inter, base + 4)]):
+                n = N * K
+                w = nf4.NF4Weight(torch.randint(0, 256, (n // 2,), dtype=torch.uint8, device=dev(), generator=g),
+                                  torch.randint(0, 256, (n // 64,), dtype=torch.uint8, device=dev(), generator=g),
+                                  (torch.rand((n // 64 + 255) // 256, device=dev(), generator=g) * 0.04 + 0.01).half(),
+                                  code2, 0.01, n, (N, K), 64, 256)
+                nodes.append(dict(weight=w, y=torch.empty((batch, N), dtype=torch.bfloat16, device=dev()),
+                                  bias=None, input=src))
+        x = torch.randn((batch, h), device=dev(), generator=g).to(torch.bfloat16)
+        step = nf4.DecodeStep(nodes, x)
+        assert step.kernel_count() == 8, (model, batch)
+        step.launch()
+        torch.cuda.synchronize()
+        assert nf4.nf4_device_error_flags() == 0
+        step.close()
 
 
 def test_small_and_fallback_node_groups():

@@ -52,6 +52,8 @@ _lib.nf4_step_create.argtypes = [ctypes.POINTER(_GemvNode), _I32, _P, _I32, ctyp
 _lib.nf4_step_create.restype = ctypes.c_int
 _lib.nf4_step_launch.argtypes = [_P, _P]
 _lib.nf4_step_launch.restype = ctypes.c_int
+_lib.nf4_step_kernel_count.argtypes = [_P, ctypes.POINTER(_I32)]
+_lib.nf4_step_kernel_count.restype = ctypes.c_int
 _lib.nf4_step_destroy.argtypes = [_P]
 _lib.nf4_step_destroy.restype = ctypes.c_int
 _lib.nf4_quantize_workspace_size.argtypes = [_I64, _I32, _I32]
@@ -256,6 +258,12 @@ class DecodeStep:
 
     def launch(self, stream=None) -> None:
         _check(_lib.nf4_step_launch(self._h, _stream(stream)), "nf4_step_launch")
+
+    def kernel_count(self) -> int:
+        """Kernel launches per replay (grouped nodes share one)."""
+        n = _I32(0)
+        _check(_lib.nf4_step_kernel_count(self._h, ctypes.byref(n)), "nf4_step_kernel_count")
+        return int(n.value)
 
     def close(self) -> None:
         if getattr(self, "_h", None) is not None and self._h.value:

@@ -422,6 +422,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_b1_kernel(const B1Args p) {
 }
 
 
+// Shared memory: the pair table (and the binary16 x in the upper halves of
+// its rows) at shared window address 64 KB; the small arrays [code2 | absmax2
+// | x scales | absmax_q | scales | partial sums | bias] below it when they
+// fit, else above it. The dynamic window starts after the per-block reserved
+// shared memory (the kernel has no static shared variables).
 bool plan_b1(const SubTensor* subs, int nsub, int64_t K, const uint16_t* x, int cb, int threads,
              int sms, B1Plan* plan) {
   const int kWarps = threads / 32;
@@ -466,10 +471,17 @@ bool plan_b1(const SubTensor* subs, int nsub, int64_t K, const uint16_t* x, int 
   p->off_bias = off;
   if (any_bias(subs, nsub)) off += align_up_u32(uint32_t(max_rows * 4), 128);
   const uint32_t tab = 65536u - uint32_t(res);
-  if (off > tab) return false;
+  uint32_t base = 0;
+  if (!place_small_arrays(off, tab, &base, &plan->smem_bytes)) return false;
+  p->off_c2 += base;
+  p->off_a2 += base;
+  p->off_xs += base;
+  p->off_q += base;
+  p->off_scale += base;
+  p->off_part += base;
+  p->off_bias += base;
   p->off_tab = tab;
-  plan->smem_bytes = tab + kTabBytes;
-  return plan->smem_bytes <= uint32_t(kMaxSmemPerCta);
+  return true;
 }
 
 template <int CB, int NT, int NSUB>

@@ -246,6 +246,17 @@ int reserved_smem_per_block() {
   });
 }
 
+// Where the planners put the small per-CTA arrays (code2, scales, partial
+// sums, ...; `bytes` in total, offsets counted from 0): below the pair table
+// at shared window address 64 KB (`tab` bytes from the start of dynamic
+// shared memory) when they fit there, else right above it. Sets the offset
+// to add to each array and the dynamic shared memory of the launch.
+bool place_small_arrays(uint32_t bytes, uint32_t tab, uint32_t* base, uint32_t* total) {
+  *base = bytes <= tab ? 0u : tab + kTabBytes;
+  *total = bytes <= tab ? tab + kTabBytes : *base + bytes;
+  return *total <= uint32_t(kMaxSmemPerCta);
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace

@@ -367,7 +367,10 @@ __global__ void __launch_bounds__(NT, 1) gemv_bn_kernel(const BNArgs p) {
   }
 }
 
-// Plan for BP vectors, CB-byte chunks and nt threads (one CTA per SM).
+// Plan for BP vectors, CB-byte chunks and nt threads (one CTA per SM): the
+// binary32 pair table at shared window address 64 KB, the small arrays
+// [code2 | absmax2 | absmax_q | scales | partial sums | bias] below it when
+// they fit, else above it.
 bool plan_bn(const SubTensor* subs, int nsub, int64_t K, const uint16_t* x, int batch, int bp,
              int cb, int nt, int sms, BNArgs* p, int* grid, uint32_t* smem_bytes) {
   const int warps = nt / 32;
@@ -418,10 +421,16 @@ bool plan_bn(const SubTensor* subs, int nsub, int64_t K, const uint16_t* x, int 
   p->off_bias = off;
   if (any_bias(subs, nsub)) off += align_up_u32(uint32_t(max_rows * 4), 128);
   const uint32_t tab = 65536u - uint32_t(res);
-  if (off > tab) return false;
+  uint32_t base = 0;
+  if (!place_small_arrays(off, tab, &base, smem_bytes)) return false;
+  p->off_c2 += base;
+  p->off_a2 += base;
+  p->off_q += base;
+  p->off_scale += base;
+  p->off_part += base;
+  p->off_bias += base;
   p->off_tab = tab;
-  *smem_bytes = tab + kTabBytes;
-  return *smem_bytes <= uint32_t(kMaxSmemPerCta);
+  return true;
 }
 
 template <int BP, int CB, int NSUB, int NT>

@@ -152,6 +152,27 @@ nf4_status nf4_step_launch(nf4_step_t step, nf4_stream_t stream) {
   return nf4::status_of(cudaGraphLaunch(step->exec, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+nf4_status nf4_step_kernel_count(nf4_step_t step, int32_t* count) {
+  if (!step || !count) return NF4_ERR_NULL;
+  *count = 0;
+  if (!step->graph) return NF4_OK;
+  size_t n = 0;
+  cudaError_t e = cudaGraphGetNodes(step->graph, nullptr, &n);
+  if (e != cudaSuccess) return nf4::status_of(e);
+  std::vector<cudaGraphNode_t> nodes(n);
+  if (n > 0) e = cudaGraphGetNodes(step->graph, nodes.data(), &n);
+  if (e != cudaSuccess) return nf4::status_of(e);
+  int32_t kernels = 0;
+  for (size_t i = 0; i < n; ++i) {
+    cudaGraphNodeType type;
+    e = cudaGraphNodeGetType(nodes[i], &type);
+    if (e != cudaSuccess) return nf4::status_of(e);
+    if (type == cudaGraphNodeTypeKernel) ++kernels;
+  }
+  *count = kernels;
+  return NF4_OK;
+}
+
 nf4_status nf4_step_destroy(nf4_step_t step) {
   if (!step) return NF4_OK;
   destroy_graph(step);
