@@ -324,16 +324,24 @@ def run_native(args, rank, world, local_rank):
         torch.cuda.empty_cache()
         gen = torch.Generator(device=dev)
         gen.manual_seed(4243)
-        st = decode_step(dev, gen, code2, 1, "llama-7b")
-        us = st["time"](reps=3, m=20)
-        gbs = st["weight_bytes"] / us / 1e3
-        result["decode_step"] = {
-            "model": "llama-7b-shaped (32 layers: q/k/v, o 4096x4096; gate/up 11008x4096; down "
-                     "4096x11008)", "batch": 1, "us_per_step": round(us, 1),
-            "us_per_linear": round(us / st["linears"], 3), "launches_per_step": st["launches"],
-            "weight_bytes": st["weight_bytes"], "gbs": round(gbs, 1),
-            "frac_of_measured_hbm": round(gbs / peak, 4)}
-        st["close"]()
+        steps = {}
+        for model, desc in (("llama-7b", "llama-7b-shaped (32 layers: q/k/v, o 4096x4096; gate/up 11008x4096; "
+                                         "down 4096x11008)"),
+                            ("qwen2.5-1.5b", "qwen2.5-1.5b-shaped (28 layers: q/o 1536x1536, k/v 256x1536 with "
+                                             "bias; gate/up 8960x1536; down 1536x8960)")):
+            st = decode_step(dev, gen, code2, 1, model)
+            us = st["time"](reps=3, m=20)
+            gbs = st["weight_bytes"] / us / 1e3
+            steps[model] = {
+                "model": desc, "batch": 1, "us_per_step": round(us, 1),
+                "us_per_linear": round(us / st["linears"], 3), "launches_per_step": st["launches"],
+                "weight_bytes": st["weight_bytes"], "gbs": round(gbs, 1),
+                "frac_of_measured_hbm": round(gbs / peak, 4)}
+            st["close"]()
+            del st
+            torch.cuda.empty_cache()
+        result["decode_step"] = steps["llama-7b"]
+        result["decode_step_qwen"] = steps["qwen2.5-1.5b"]
     if rank == 0 and world == 1 and not args.no_layers:
         # every GEMV layer shape of the configurations, timed on its own
         # (after the timed region; graphs of back-to-back launches over > 4x L2)
