@@ -344,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_b1_kernel(const B1Args p) {
       if (pc < npieces) {
         const int ch = pc / kPiecesPerChunk;
         const int within = pc - ch * kPiecesPerChunk;
-        *reinterpret_cast<uint4*>(tab + x16_offset<CB>(ch) + uint32_t(within) * 16u) =
+        *reinterpret_cast<uint4*>(tab + x16_slot(ch, within, p.cpr)) =
             make_uint4(h[0], h[1], h[2], h[3]);
         if (within == 0) sXs[ch] = __uint_as_float(uint32_t(127 + e) << 23);
         x_exact = x_exact && ex;
@@ -390,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_b1_kernel(const B1Args p) {
 #pragma unroll
     for (int q = 0; q < CE / 8; ++q) {
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (act) v = lds_u128(L.tab_s + x16_offset<CB>(cc) + uint32_t(q) * 16u);
+      if (act) v = lds_u128(L.tab_s + x16_slot(cc, q, p.cpr));
       L.x16[4 * q + 0] = v.x;
       L.x16[4 * q + 1] = v.y;
       L.x16[4 * q + 2] = v.z;

@@ -194,12 +194,15 @@ __device__ __forceinline__ int group_row0(int nrows, int G, int g) {
   return q * g + (g < r ? g : r);
 }
 
-// Shared offset of the binary16 x chunk c: the upper 128 bytes of table rows,
-// 32 / CB chunks of 4 * CB bytes per row.
-template <int CB>
-__device__ __forceinline__ uint32_t x16_offset(int c) {
-  constexpr int per_row = 32 / CB;
-  return uint32_t(c / per_row) * 256u + 128u + uint32_t(c % per_row) * uint32_t(4 * CB);
+// Shared offset of piece q (16 bytes: 8 binary16 values) of the binary16 x
+// chunk c in the upper 128 bytes of the table rows: 16-byte unit
+// m = q * cpr + c, eight units per row half. A warp writing consecutive pieces,
+// or reading piece q of consecutive chunks, covers whole 128-byte row halves,
+// so neither access has bank conflicts (chunk-major units put every even lane
+// of a read on the same four banks). K <= 16384 keeps m below 2048.
+__device__ __forceinline__ uint32_t x16_slot(int c, int q, int cpr) {
+  const uint32_t m = uint32_t(q) * uint32_t(cpr) + uint32_t(c);
+  return (m >> 3) * 256u + 128u + (m & 7u) * 16u;
 }
 
 // One step of RPG rows of this lane's column chunk, held in registers.
