@@ -1,4 +1,4 @@
-// nf4_gemv_stream.cu -- batch-1 decode GEMV y = W_hat x with the NF4 double-quant
+// nf4_gemv_b1.cu -- batch-1 decode GEMV y = W_hat x with the NF4 double-quant
 // dequantization fused, for sm_103a.
 //
 // What is computed follows "RTX 4060 上的 LLM 量化实测：4-bit decode 比 FP16 慢在
@@ -34,9 +34,10 @@
 //     binary32 accumulation.
 //   * x is converted once per CTA into binary16 after an exact power-of-two
 //     scaling per column chunk (the upper halves of the table rows hold the
-//     converted chunks); a CTA whose x does not convert exactly (dynamic range
-//     beyond binary16, NaN/Inf) uses binary32 x with conversions of the codes
-//     and packed fma.rn.f32x2 instead. The codes carry a binary16 rounding
+//     converted chunks, piece-major so that neither the stores nor the
+//     per-lane read-back has bank conflicts); a CTA whose x does not convert
+//     exactly (dynamic range beyond binary16, NaN/Inf) uses binary32 x with
+//     conversions of the codes and packed fma.rn.f32x2 instead. The codes carry a binary16 rounding
 //     error of at most 3.3e-4 relative, inside the GEMV tolerance.
 //   * Per-warp partial sums of each row go to shared memory; the group's
 //     threads add them in warp order (deterministic, no atomics).

@@ -23,9 +23,7 @@ __device__ __forceinline__ SubTensor pick_sub(const SubTensor (&s)[kMaxSub], int
 constexpr uint32_t kTabBytes = 65536;  // 256 rows of 256 B
 constexpr int kMaxSmemPerCta = 227 * 1024;
 
-// Everything a launch needs, in one argument block. A launch serves one to
-// kMaxSub weights that share x (a grouped launch): CTAs [cta0, cta0 + ctas)
-
+// True when any weight of a grouped launch has a bias.
 bool any_bias(const SubTensor* subs, int nsub) {
   for (int j = 0; j < nsub; ++j)
     if (subs[j].out.bias) return true;
@@ -233,9 +231,6 @@ __device__ __forceinline__ void load_step(Step<CB, RPG>& st, const uint8_t* p, u
   }
 }
 
-// Dot product of one row's chunk (CB packed bytes in w) with the lane's x
-// chunk. kFast: binary16 x (pre-scaled) and mixed-precision FMAs on the
-// binary16 code pairs; otherwise binary32 x and packed binary32 FMAs.
 uint32_t align_up_u32(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
 int reserved_smem_per_block() {
