@@ -48,10 +48,12 @@ __device__ __forceinline__ float2 lds_f2(uint32_t addr) {
 // with the block scale applied once the lanes of one quantization block
 // (32 / CB adjacent lanes: blocks of at least 64 elements) have been summed;
 // partial added to (or stored in, for the first slice)
-// sPart[(row * BP + vector) * W + warp].
+// sPart[warp * pstride + row * BP + vector] (warp-major: the lanes storing a
+// step's partials, and the threads summing a slot over the warps, touch
+// consecutive words).
 template <int BP, int CB, int RPG>
 __device__ __forceinline__ void compute_step_n(const Step<CB, RPG>& st, const LaneN<BP, CB>& L,
-                                               const float* sScale, float* sPart, int spr, int W,
+                                               const float* sScale, float* sPart, int spr, int pstride,
                                                int wg, int lane, int r0, int rows, bool first) {
   constexpr int V = RPG * BP;
   // lanes of one 64-element block: 32 / CB (2^kPre); log2(V) transposed steps
@@ -115,7 +117,7 @@ __device__ __forceinline__ void compute_step_n(const Step<CB, RPG>& st, const La
     const int idx = transposed_index<RPG * BP>(lane);
     const int r = idx / BP, b = idx - (idx / BP) * BP;
     if (r < rows) {
-      float* d = sPart + ((r0 + r) * BP + b) * W + wg;
+      float* d = sPart + wg * pstride + (r0 + r) * BP + b;
       *d = first ? red : *d + red;
     }
   }
@@ -125,22 +127,22 @@ template <int BP, int CB, int RPG>
 __device__ __forceinline__ void consume_n(const uint8_t* lane_src, uint32_t row_bytes,
                                           Step<CB, RPG>& A, Step<CB, RPG>& B, Step<CB, RPG>& C,
                                           const LaneN<BP, CB>& L, const float* sScale, float* sPart,
-                                          int spr, int W, int wg, int lane, int rg0, int rg1,
+                                          int spr, int pstride, int wg, int lane, int rg0, int rg1,
                                           bool first) {
   const int n = rg1 - rg0;
   const int ns = (n + RPG - 1) / RPG;
   auto rows_of = [&](int s) { return (n - s * RPG < RPG) ? n - s * RPG : RPG; };
   auto src_of = [&](int s) { return lane_src + uint32_t(rg0 + s * RPG) * row_bytes; };
   for (int s = 0; s < ns; s += 3) {
-    compute_step_n<BP, CB, RPG>(A, L, sScale, sPart, spr, W, wg, lane, rg0 + s * RPG, rows_of(s), first);
+    compute_step_n<BP, CB, RPG>(A, L, sScale, sPart, spr, pstride, wg, lane, rg0 + s * RPG, rows_of(s), first);
     if (s + 3 < ns) load_step<CB, RPG>(A, src_of(s + 3), row_bytes, rows_of(s + 3));
     if (s + 1 < ns) {
-      compute_step_n<BP, CB, RPG>(B, L, sScale, sPart, spr, W, wg, lane, rg0 + (s + 1) * RPG,
+      compute_step_n<BP, CB, RPG>(B, L, sScale, sPart, spr, pstride, wg, lane, rg0 + (s + 1) * RPG,
                                   rows_of(s + 1), first);
       if (s + 4 < ns) load_step<CB, RPG>(B, src_of(s + 4), row_bytes, rows_of(s + 4));
     }
     if (s + 2 < ns) {
-      compute_step_n<BP, CB, RPG>(C, L, sScale, sPart, spr, W, wg, lane, rg0 + (s + 2) * RPG,
+      compute_step_n<BP, CB, RPG>(C, L, sScale, sPart, spr, pstride, wg, lane, rg0 + (s + 2) * RPG,
                                   rows_of(s + 2), first);
       if (s + 5 < ns) load_step<CB, RPG>(C, src_of(s + 5), row_bytes, rows_of(s + 5));
     }
@@ -153,27 +155,27 @@ template <int BP, int CB, int RPG>
 __device__ __forceinline__ void consume_n4(const uint8_t* lane_src, uint32_t row_bytes,
                                            Step<CB, RPG>& A, Step<CB, RPG>& B, Step<CB, RPG>& C,
                                            Step<CB, RPG>& D, const LaneN<BP, CB>& L,
-                                           const float* sScale, float* sPart, int spr, int W, int wg,
+                                           const float* sScale, float* sPart, int spr, int pstride, int wg,
                                            int lane, int rg0, int rg1, bool first) {
   const int n = rg1 - rg0;
   const int ns = (n + RPG - 1) / RPG;
   auto rows_of = [&](int s) { return (n - s * RPG < RPG) ? n - s * RPG : RPG; };
   auto src_of = [&](int s) { return lane_src + uint32_t(rg0 + s * RPG) * row_bytes; };
   for (int s = 0; s < ns; s += 4) {
-    compute_step_n<BP, CB, RPG>(A, L, sScale, sPart, spr, W, wg, lane, rg0 + s * RPG, rows_of(s), first);
+    compute_step_n<BP, CB, RPG>(A, L, sScale, sPart, spr, pstride, wg, lane, rg0 + s * RPG, rows_of(s), first);
     if (s + 4 < ns) load_step<CB, RPG>(A, src_of(s + 4), row_bytes, rows_of(s + 4));
     if (s + 1 < ns) {
-      compute_step_n<BP, CB, RPG>(B, L, sScale, sPart, spr, W, wg, lane, rg0 + (s + 1) * RPG,
+      compute_step_n<BP, CB, RPG>(B, L, sScale, sPart, spr, pstride, wg, lane, rg0 + (s + 1) * RPG,
                                   rows_of(s + 1), first);
       if (s + 5 < ns) load_step<CB, RPG>(B, src_of(s + 5), row_bytes, rows_of(s + 5));
     }
     if (s + 2 < ns) {
-      compute_step_n<BP, CB, RPG>(C, L, sScale, sPart, spr, W, wg, lane, rg0 + (s + 2) * RPG,
+      compute_step_n<BP, CB, RPG>(C, L, sScale, sPart, spr, pstride, wg, lane, rg0 + (s + 2) * RPG,
                                   rows_of(s + 2), first);
       if (s + 6 < ns) load_step<CB, RPG>(C, src_of(s + 6), row_bytes, rows_of(s + 6));
     }
     if (s + 3 < ns) {
-      compute_step_n<BP, CB, RPG>(D, L, sScale, sPart, spr, W, wg, lane, rg0 + (s + 3) * RPG,
+      compute_step_n<BP, CB, RPG>(D, L, sScale, sPart, spr, pstride, wg, lane, rg0 + (s + 3) * RPG,
                                   rows_of(s + 3), first);
       if (s + 7 < ns) load_step<CB, RPG>(D, src_of(s + 7), row_bytes, rows_of(s + 7));
     }
@@ -237,6 +239,7 @@ __global__ void __launch_bounds__(NT, 1) gemv_bn_kernel(const BNArgs p) {
   const int64_t row_begin = (bid * N) / sb.ctas;
   const int64_t row_end = ((bid + 1) * N) / sb.ctas;
   const int nrows = int(row_end - row_begin);
+  const int pstride = nrows * BP;  // partial-sum slots of one warp
   const int64_t b0 = (row_begin * K) >> t.lbs;
   const int nq = nrows * p.spr;
   const int64_t g0 = b0 >> t.ls2;
@@ -348,10 +351,10 @@ __global__ void __launch_bounds__(NT, 1) gemv_bn_kernel(const BNArgs p) {
       }
     }
     if constexpr (NT == 256)
-      consume_n4<BP, CB, RPG>(lane_src, rb, A, B, C, D, L, sScale, sPart, p.spr, p.W, wg, lane, rg0,
+      consume_n4<BP, CB, RPG>(lane_src, rb, A, B, C, D, L, sScale, sPart, p.spr, pstride, wg, lane, rg0,
                               rg1, sl == 0);
     else
-      consume_n<BP, CB, RPG>(lane_src, rb, A, B, C, L, sScale, sPart, p.spr, p.W, wg, lane, rg0, rg1,
+      consume_n<BP, CB, RPG>(lane_src, rb, A, B, C, L, sScale, sPart, p.spr, pstride, wg, lane, rg0, rg1,
                              sl == 0);
   }
 
@@ -362,7 +365,7 @@ __global__ void __launch_bounds__(NT, 1) gemv_bn_kernel(const BNArgs p) {
     const int r = rg0 + idx / BP, b = idx - (idx / BP) * BP;
     if (b >= p.batch) continue;
     float v = 0.0f;
-    for (int w = 0; w < p.W; ++w) v += sPart[(r * BP + b) * p.W + w];
+    for (int w = 0; w < p.W; ++w) v += sPart[w * pstride + r * BP + b];
     y_store(sb.out, int64_t(b) * N + row_begin + r, v, has_bias ? sBias[r] : 0u);
   }
 }
