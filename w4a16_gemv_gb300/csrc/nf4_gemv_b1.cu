@@ -335,12 +335,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_b1_kernel(const B1Args p) {
       bool ex = mb < 0x7f80u;
       uint32_t h[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < 4; ++q) {  // one packed conversion per pair, checked by converting back
         const float f0 = __fmul_rn(__uint_as_float(w[q] << 16), down);
         const float f1 = __fmul_rn(__uint_as_float(w[q] & 0xffff0000u), down);
-        const __half h0 = __float2half_rn(f0), h1 = __float2half_rn(f1);
-        ex = ex && (__half2float(h0) == f0) && (__half2float(h1) == f1);
-        h[q] = uint32_t(__half_as_ushort(h0)) | (uint32_t(__half_as_ushort(h1)) << 16);
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h[q]) : "f"(f1), "f"(f0));  // f0 in the low half
+        const float2 back = __half22float2(*reinterpret_cast<const __half2*>(&h[q]));
+        ex = ex && (back.x == f0) && (back.y == f1);
       }
       if (pc < npieces) {
         const int ch = pc / kPiecesPerChunk;
