@@ -229,8 +229,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_b1_kernel(const B1Args p) {
   const int c = wg * 32 + lane;
   const bool act = consumer && c < p.cpr;
   const int cc = act ? c : p.cpr - 1;
-  const int rg0 = consumer ? group_row0(nrows, p.G, g) : 0;
-  const int rg1 = consumer ? group_row0(nrows, p.G, g + 1) : 0;
+  const int rg0 = consumer ? group_row0<RPG>(nrows, p.G, g) : 0;
+  const int rg1 = consumer ? group_row0<RPG>(nrows, p.G, g + 1) : 0;
   const uint8_t* lane_src = slab + int64_t(cc) * CB;
 
   pdl_wait_prior_grid();

@@ -186,10 +186,16 @@ __device__ __forceinline__ int transposed_index(int lane) {
   return r;
 }
 
-// First row (relative to the CTA) of row group g: balanced contiguous split.
+// First row (relative to the CTA) of row group g: contiguous ranges of whole
+// steps of RPG rows, the last groups taking the remainder. The largest group
+// has as many steps as in an even split, and the others compute no padding
+// rows (an even split of 27 rows over 4 groups computes 32 row slots, this
+// one 28).
+template <int RPG>
 __device__ __forceinline__ int group_row0(int nrows, int G, int g) {
-  const int q = nrows / G, r = nrows - q * G;
-  return q * g + (g < r ? g : r);
+  const int per = ((nrows + G - 1) / G + RPG - 1) / RPG * RPG;
+  const int r = per * g;
+  return r < nrows ? r : nrows;
 }
 
 // Shared offset of piece q (16 bytes: 8 binary16 values) of the binary16 x

@@ -249,8 +249,8 @@ __global__ void __launch_bounds__(NT, 1) gemv_bn_kernel(const BNArgs p) {
   const int g = warp / p.W;
   const int wg = warp - g * p.W;
   const bool consumer = g < p.G;
-  const int rg0 = consumer ? group_row0(nrows, p.G, g) : 0;
-  const int rg1 = consumer ? group_row0(nrows, p.G, g + 1) : 0;
+  const int rg0 = consumer ? group_row0<RPG>(nrows, p.G, g) : 0;
+  const int rg1 = consumer ? group_row0<RPG>(nrows, p.G, g + 1) : 0;
   pdl_wait_prior_grid();
 
   // Small loads first (ordered), then the stores that consume them.
