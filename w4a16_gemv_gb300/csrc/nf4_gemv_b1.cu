@@ -79,19 +79,17 @@ __device__ __forceinline__ float row_dot(const uint32_t (&w)[CB / 4], uint32_t l
                                          uint32_t tab_s, uint32_t lane4, const uint32_t (&x16)[CB],
                                          const float2 (&xf)[CB]) {
   if constexpr (kFast) {
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    float a0 = 0.f, a1 = 0.f;
 #pragma unroll
     for (int wi = 0; wi < CB / 4; ++wi) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const uint32_t addr = __byte_perm(w[wi], lanebase, 0x7604u | (uint32_t(i) << 4));
         const uint32_t h = lds_u32(addr);
-        const int k = 4 * wi + i;
-        if (i & 1) fma2_f16_f32(h, x16[k], a2, a3);
-        else fma2_f16_f32(h, x16[k], a0, a1);
+        fma2_f16_f32(h, x16[4 * wi + i], a0, a1);
       }
     }
-    return (a0 + a1) + (a2 + a3);
+    return a0 + a1;
   } else {
     float2 pa = make_float2(0.f, 0.f), pb = make_float2(0.f, 0.f);
 #pragma unroll
@@ -118,7 +116,6 @@ struct Lane {
   bool act;  // this lane owns a real chunk
   int scol;  // quantization block of the chunk within a row
   const float* sScale;  // decoded scale of block i of the CTA (i = row * spr + scol)
-  __device__ __forceinline__ float scale(int i) const { return sScale[i]; }
 };
 
 // Computes one step (rows r0 .. r0 + rows - 1 of the CTA) from registers,
@@ -130,12 +127,15 @@ __device__ __forceinline__ void compute_step(const Step<CB, RPG>& st, const Lane
   // One code path for full and partial steps (a second path for the last
   // step made the loop body too large for the instruction cache): rows past
   // the end are computed from stale registers and dropped.
+  // The decoded scales of rows r0 .. r0 + RPG - 1 for this lane's block;
+  // rows past the CTA's end read the padding after the scale array (their
+  // values are dropped at the store, and the reduction never mixes rows).
+  const float* srow = L.sScale + (r0 * spr + L.scol);
   float part[RPG];
 #pragma unroll
   for (int r = 0; r < RPG; ++r) {
     const float sum = row_dot<CB, kFast>(st.w[r], L.lanebase, L.tab_s, L.lane4, L.x16, L.xf);
-    part[r] = (L.act && r < rows) ? __fmul_rn(L.scale((r0 + (r < rows ? r : 0)) * spr + L.scol), L.xs) * sum
-                                  : 0.0f;
+    part[r] = L.act ? __fmul_rn(srow[r * spr], L.xs) * sum : 0.0f;
   }
   const float red = transposed_warp_reduce<RPG>(part, lane);
   if (lane < RPG) {
@@ -465,8 +465,8 @@ bool plan_b1(const SubTensor* subs, int nsub, int64_t K, const uint16_t* x, int 
   p->off_q = off;
   if (max_nq > int64_t(4) * threads * 16) return false;  // one batch of 16-byte loads
   off += align_up_u32(uint32_t(max_nq + 16), 128);
-  p->off_scale = off;
-  off += align_up_u32(uint32_t(max_nq * 4), 128);
+  p->off_scale = off;  // + one step of padding rows (read for dropped rows)
+  off += align_up_u32(uint32_t((max_nq + int64_t(NF4_B1_RPG) * p->spr) * 4), 128);
   p->off_part = off;
   off += align_up_u32(uint32_t(max_rows * W * 4), 128);
   p->off_bias = off;
