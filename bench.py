@@ -492,6 +492,26 @@ def _sample_rows(t, x_host, budget_s):
     return max(1, min(N_ROWS, int(budget_s / per_row)))
 
 
+def host_cpu():
+    """The host's usable core count and a CPU description (the model name on
+    x86, implementer/part codes on Arm), for the CPU-oracle figures."""
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    desc = ""
+    try:
+        fields = {}
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields.setdefault(k.strip(), v.strip())
+        desc = fields.get("model name") or " ".join(
+            f"{k} {fields[k]}" for k in ("CPU implementer", "CPU part") if k in fields)
+    except OSError:
+        pass
+    import platform
+    return {"host_cores": cores, "cpu": desc or platform.machine()}
+
+
 def cpu_baseline(args, q, x_host, bytes_):
     t, x_host = _oracle_inputs(q, x_host)
     rows = _sample_rows(t, x_host, 2.0)
@@ -507,7 +527,7 @@ def cpu_baseline(args, q, x_host, bytes_):
     v = sum(bytes_.values()) * frac * reps / dt / 1e9
     return {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"first {rows} of {N_ROWS} rows per step (dequant bf16 + fp16 + fp64 GEMV), "
-                      f"{reps} steps in {dt:.1f} s, single-threaded C oracle"}
+                      f"{reps} steps in {dt:.1f} s, single-threaded C oracle", **host_cpu()}
 
 
 def run_reference(args):
@@ -532,7 +552,7 @@ def run_reference(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "impl": "reference", "config": {"workload": WORKLOAD, "parallelism": "single CPU core"},
             "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": sample},
+                             "sample": sample, **host_cpu()},
             "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
