@@ -320,13 +320,11 @@ NF4_API nf4_status nf4_quantize(const float* w, int64_t n, int32_t blocksize, in
  *     exceed NF4_QUANTIZE_NOALLOC_SCRATCH_BYTES (n <= 2^28 at blocksize 64,
  *     s2_blocksize 256); larger inputs return NF4_ERR_WORKSPACE before any
  *     CUDA call.
- *   Set-up: the first call on each device (with that device current) looks up
- *     the array's device address with cudaGetSymbolAddress and caches it; make
- *     that first call before any stream capture. The cached address belongs
- *     to the device's primary context as it was then: do not call this entry
- *     point after cudaDeviceReset on that device, or from a different context
- *     made current for it (the array would then live at another address).
- *     nf4_quantize, which takes caller memory, has no such restriction.
+ *   Set-up: every call looks up the array's device address in the current
+ *     context with cudaGetSymbolAddress (nothing is cached, so the entry point
+ *     keeps working after cudaDeviceReset or with another context current).
+ *     The first call on a device may load the library's module: make one call
+ *     before any stream capture.
  *   Concurrency: the array is shared by all callers on a device, so calls
  *     whose kernels may overlap in time (different streams, or host threads
  *     without an ordering between their streams) race on it; the caller

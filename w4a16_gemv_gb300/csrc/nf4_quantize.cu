@@ -21,7 +21,6 @@
 //   3. finalize_offset: one thread, binary64 sum of the group sums in order,
 //      divided by the block count, rounded to binary32.
 //   4. second_level: one warp per group -- absmax2 and absmax_q.
-#include <mutex>
 
 #include "nf4_internal.cuh"
 
@@ -208,29 +207,14 @@ namespace {
 
 __device__ __align__(256) unsigned char g_quantize_scratch[NF4_QUANTIZE_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mutex;
-void* g_scratch_ptr[kMaxDevices] = {};
-
 }  // namespace
 
-// Device address of g_quantize_scratch on the current device. The first call
-// on a device looks it up with cudaGetSymbolAddress (which may load this
-// translation unit's module); later calls read the per-device cache.
+// Device address of g_quantize_scratch in the current context, looked up on
+// every call (cudaGetSymbolAddress, which may load this translation unit's
+// module): nothing is cached, so the address stays right after a
+// cudaDeviceReset or when another context is current.
 cudaError_t quantize_static_scratch(void** ptr) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_quantize_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = p;
-  }
-  *ptr = g_scratch_ptr[dev];
-  return cudaSuccess;
+  return cudaGetSymbolAddress(ptr, g_quantize_scratch);
 }
 
 }  // namespace nf4
