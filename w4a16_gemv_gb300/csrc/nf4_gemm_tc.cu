@@ -28,12 +28,13 @@
 //     rounding to y's type) once. When one CTA per tile would leave many SMs
 //     idle, a cluster of three CTAs covers a pair of tiles instead.
 // Every wait on an mbarrier is bounded (about one second); a wait that runs
-// out sets bit 0 of the device error flags and the kernel still completes
-// its cluster barriers and frees its tensor memory. That path only reports a
-// hang: copies or MMAs that never completed may still be in flight into the
-// CTA's shared or tensor memory when it exits, so after a timeout the
-// launch's results, and the device's state, are undefined. The limit is long
-// enough that only a real hang reaches it.
+// out sets bit 0 of the device error flags, and the kernel still completes
+// its cluster barriers, waits (with the same bound) for its own copies and
+// MMAs still in flight, frees its tensor memory and exits. That path reports
+// a hang rather than recovering from it: the launch's results are undefined,
+// and a copy or MMA that never completes within the second wait may still be
+// in flight when the CTA exits. The limit is long enough that only a real
+// hang reaches it.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -530,6 +531,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   }
 
+  // After a wait that ran out, copies or MMAs of this CTA may still be in
+  // flight: wait for them (with the same bound) before the tensor memory is
+  // freed and the shared memory released. The last commit covers every
+  // earlier MMA; a ring slot's last copy is the one of the last stage using it.
+  if (__syncthreads_or(!ok) && warp == kCopyWarp && lane == 0) {
+    if (ns > 0) wait_mma_done(ns - 1);
+    for (int st = ns > kRing ? ns - kRing : 0; st < ns; ++st)
+      mbar_wait_bounded(&full[st % kRing], uint32_t((st / kRing) & 1), kWaitLimitCycles);
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
