@@ -213,8 +213,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_b1_kernel(const B1Args p) {
 
   const int64_t row_bytes = K >> 1;
   const int64_t bid = int64_t(blockIdx.x) - sb.cta0;
-  const int64_t row_begin = (bid * N) / sb.ctas;
-  const int64_t row_end = ((bid + 1) * N) / sb.ctas;
+  int64_t row_begin, row_end;
+  cta_rows(bid, sb.ctas, N, &row_begin, &row_end);
   const int nrows = int(row_end - row_begin);
   const int64_t b0 = (row_begin * K) >> t.lbs;  // first quantization block of the CTA
   const int nq = nrows * p.spr;
@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_b1_kernel(const B1Args p) {
   const uint8_t* slab = t.packed + row_begin * row_bytes;
 
   // This thread's place among the consumers.
-  const int g = warp / p.W;
+  const int g = int(uint32_t(warp) / uint32_t(p.W));
   const int wg = warp - g * p.W;
   const bool consumer = g < p.G;
   const int c = wg * 32 + lane;

@@ -190,12 +190,28 @@ __device__ __forceinline__ int transposed_index(int lane) {
 // steps of RPG rows, the last groups taking the remainder. The largest group
 // has as many steps as in an even split, and the others compute no padding
 // rows (an even split of 27 rows over 4 groups computes 32 row slots, this
-// one 28).
+// one 28). Unsigned 32-bit division (cheaper than signed).
 template <int RPG>
 __device__ __forceinline__ int group_row0(int nrows, int G, int g) {
-  const int per = ((nrows + G - 1) / G + RPG - 1) / RPG * RPG;
-  const int r = per * g;
-  return r < nrows ? r : nrows;
+  const uint32_t per = ((uint32_t(nrows) + uint32_t(G) - 1u) / uint32_t(G) + RPG - 1) / RPG * RPG;
+  const uint32_t r = per * uint32_t(g);
+  return r < uint32_t(nrows) ? int(r) : nrows;
+}
+
+// Rows [*first, *end) of CTA `bid` of `ctas` over N rows (balanced split),
+// in 32-bit unsigned arithmetic whenever ctas * N fits in 32 bits (every
+// practical shape: a 64-bit division costs several times as many
+// instructions), else in 64-bit.
+__device__ __forceinline__ void cta_rows(int64_t bid, int ctas, int64_t N, int64_t* first,
+                                         int64_t* end) {
+  if (N <= int64_t(0xffffffffu) / ctas) {
+    const uint32_t b = uint32_t(bid), n = uint32_t(N), c = uint32_t(ctas);
+    *first = (b * n) / c;
+    *end = ((b + 1u) * n) / c;
+  } else {
+    *first = (bid * N) / ctas;
+    *end = ((bid + 1) * N) / ctas;
+  }
 }
 
 // Shared offset of piece q (16 bytes: 8 binary16 values) of the binary16 x

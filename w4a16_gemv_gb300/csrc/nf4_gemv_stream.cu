@@ -236,8 +236,8 @@ __global__ void __launch_bounds__(NT, 1) gemv_bn_kernel(const BNArgs p) {
 
   const int64_t row_bytes = K >> 1;
   const int64_t bid = int64_t(blockIdx.x) - sb.cta0;
-  const int64_t row_begin = (bid * N) / sb.ctas;
-  const int64_t row_end = ((bid + 1) * N) / sb.ctas;
+  int64_t row_begin, row_end;
+  cta_rows(bid, sb.ctas, N, &row_begin, &row_end);
   const int nrows = int(row_end - row_begin);
   const int pstride = nrows * BP;  // partial-sum slots of one warp
   const int64_t b0 = (row_begin * K) >> t.lbs;
@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(NT, 1) gemv_bn_kernel(const BNArgs p) {
   const int ng = nq > 0 ? int(((b0 + nq - 1) >> t.ls2) - g0 + 1) : 0;
   const uint8_t* slab = t.packed + row_begin * row_bytes;
 
-  const int g = warp / p.W;
+  const int g = int(uint32_t(warp) / uint32_t(p.W));
   const int wg = warp - g * p.W;
   const bool consumer = g < p.G;
   const int rg0 = consumer ? group_row0<RPG>(nrows, p.G, g) : 0;
