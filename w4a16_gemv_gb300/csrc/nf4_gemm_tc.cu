@@ -240,6 +240,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     fence_mbar_init();
   }
+  // Programmatic dependent launch: the next kernel may be scheduled now; this
+  // one reads no global memory before the grid-dependency wait below (TMEM,
+  // barriers and the pair table need none).
+  pdl_allow_dependents();
+
+  // Lane-private pair table: row e (256 B) holds (NF4[e >> 4], NF4[e & 15])
+  // for lane l at bytes 8l..8l+7 (no bank conflicts).
+  {
+    const float my_code = nf4_code_select(lane & 15);
+    unsigned char* tabp = smem + p.off_tab;
+    for (int i = tid; i < 256 * 16; i += kTcThreads) {
+      const int e = i >> 4, q = i & 15;
+      const float hi = __shfl_sync(0xffffffffu, my_code, e >> 4);
+      const float lo = __shfl_sync(0xffffffffu, my_code, e & 15);
+      *reinterpret_cast<float4*>(tabp + e * 256 + q * 16) = make_float4(hi, lo, hi, lo);
+    }
+  }
 
   // Waits until the MMAs of stage j (and every earlier stage) are done: the
   // commit of stage j arrives on mdone[j % kRing]; a barrier is reused only
@@ -255,6 +272,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // i + kRing at stage i, into the registers stage i used (the loop is
   // unrolled over the ring, so no register is copied while its load is in
   // flight).
+  pdl_wait_prior_grid();
   const uint16_t c2v = tid < 256 ? __ldg(t.code2 + tid) : uint16_t(0);
   auto load_scale_in = [&](int i, uint32_t& q, uint32_t& a2) {
     q = 0u;
@@ -290,18 +308,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == kCopyWarp && lane == 0)
     for (int i = 0; i < kAhead && i < ns; ++i) issue_tiles(i);
 
-  // Lane-private pair table: row e (256 B) holds (NF4[e >> 4], NF4[e & 15])
-  // for lane l at bytes 8l..8l+7 (no bank conflicts).
-  {
-    const float my_code = nf4_code_select(lane & 15);
-    unsigned char* tabp = smem + p.off_tab;
-    for (int i = tid; i < 256 * 16; i += kTcThreads) {
-      const int e = i >> 4, q = i & 15;
-      const float hi = __shfl_sync(0xffffffffu, my_code, e >> 4);
-      const float lo = __shfl_sync(0xffffffffu, my_code, e & 15);
-      *reinterpret_cast<float4*>(tabp + e * 256 + q * 16) = make_float4(hi, lo, hi, lo);
-    }
-  }
   if (tid < 256) sC2[tid] = half_bits_to_float(c2v);
 
   tc_fence_before();
@@ -576,13 +582,15 @@ cudaError_t launch_tc(const TcArgs& a, const CUtensorMap& tmx, const CUtensorMap
   cfg.blockDim = dim3(unsigned(kTcThreads));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = unsigned(a.splits);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = NF4_USE_PDL ? 1 : 0;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, a, tmx, tmw);
 }
 
