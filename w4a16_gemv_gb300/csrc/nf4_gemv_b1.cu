@@ -11,18 +11,19 @@
 //
 // Layout of a CTA (one per SM, 16 warps):
 //   * The CTA owns a contiguous, balanced range of rows, split into G
-//     contiguous sub-ranges, one per row group of W warps; lane l of warp w of
-//     a group owns column chunk 32 w + l (CB packed bytes, 2 CB weights) of
-//     every row of its sub-range. Warps beyond G * W only help with the
-//     prologue.
+//     contiguous sub-ranges of whole RPG-row steps, one per row group of W
+//     warps; lane l of warp w of a group owns column chunk 32 w + l (CB packed
+//     bytes, 2 CB weights) of every row of its sub-range. Warps beyond G * W
+//     only help with the prologue.
 //   * Weights go straight from global memory into registers with 16-byte
 //     streaming loads (a warp reads 512 contiguous bytes of a row), RPG rows
 //     per step and three steps in flight, so no shared-memory staging is
 //     needed. (On this GPU a 1-D bulk copy costs about one memory latency of
 //     copy-engine time per copy, so copies under ~32 KB cannot stream a CTA's
 //     rows at full bandwidth.)
-//   * After the grid-dependency wait the small loads (x, code2, absmax2, absmax_q) go out together (as
-//     volatile loads, so the compiler keeps them ahead of the weight stream),
+//   * After the grid-dependency wait the small loads (x, code2, absmax2,
+//     absmax_q) go out together (as volatile loads, so the compiler keeps them
+//     ahead of the weight stream),
 //     and the first weight steps once they have arrived and x is converted
 //     (loads queue per SM, so a small load issued next to a weight stream
 //     would wait behind it); the block scales of the CTA are decoded once
@@ -37,8 +38,9 @@
 //     converted chunks, piece-major so that neither the stores nor the
 //     per-lane read-back has bank conflicts); a CTA whose x does not convert
 //     exactly (dynamic range beyond binary16, NaN/Inf) uses binary32 x with
-//     conversions of the codes and packed fma.rn.f32x2 instead. The codes carry a binary16 rounding
-//     error of at most 3.3e-4 relative, inside the GEMV tolerance.
+//     conversions of the codes and packed fma.rn.f32x2 instead. The codes
+//     carry a binary16 rounding error of at most 3.3e-4 relative, inside the
+//     GEMV tolerance.
 //   * Per-warp partial sums of each row go to shared memory; the group's
 //     threads add them in warp order (deterministic, no atomics).
 
