@@ -199,9 +199,10 @@ __device__ __forceinline__ int group_row0(int nrows, int G, int g) {
 }
 
 // Rows [*first, *end) of CTA `bid` of `ctas` over N rows (balanced split),
-// in 32-bit unsigned arithmetic whenever ctas * N fits in 32 bits (every
-// practical shape: a 64-bit division costs several times as many
-// instructions), else in 64-bit.
+// in 32-bit unsigned arithmetic whenever ctas * N fits in 32 bits (a 64-bit
+// division costs several times as many instructions). The planners' limit of
+// 32768 block scales per CTA keeps every launch of these kernels inside the
+// 32-bit branch; the 64-bit one is a guard.
 __device__ __forceinline__ void cta_rows(int64_t bid, int ctas, int64_t N, int64_t* first,
                                          int64_t* end) {
   if (N <= int64_t(0xffffffffu) / ctas) {
