@@ -17,8 +17,9 @@
 //     only help with the prologue.
 //   * Weights go straight from global memory into registers with 16-byte
 //     streaming loads (a warp reads 512 contiguous bytes of a row), RPG rows
-//     per step and three steps in flight, so no shared-memory staging is
-//     needed. (On this GPU a 1-D bulk copy costs about one memory latency of
+//     per step and two steps in flight, so no shared-memory staging is
+//     needed (three steps in flight measured 1-3% slower per layer: the
+//     larger burst of loads delays the shared-memory work behind it). (On this GPU a 1-D bulk copy costs about one memory latency of
 //     copy-engine time per copy, so copies under ~32 KB cannot stream a CTA's
 //     rows at full bandwidth.)
 //   * After the grid-dependency wait the small loads (x, code2, absmax2,
@@ -146,28 +147,22 @@ __device__ __forceinline__ void compute_step(const Step<CB, RPG>& st, const Lane
   }
 }
 
-// The consumer loop of one row group: three steps of RPG rows in flight.
+// The consumer loop of one row group: two steps of RPG rows in flight.
 template <int CB, int RPG, bool kFast>
 __device__ __forceinline__ void consume(const B1Args& p, const uint8_t* lane_src, uint32_t row_bytes,
-                                        Step<CB, RPG>& A, Step<CB, RPG>& B, Step<CB, RPG>& C,
-                                        const Lane<CB>& L, float* sPart, int wg, int lane,
-                                        int rg0, int rg1) {
+                                        Step<CB, RPG>& A, Step<CB, RPG>& B, const Lane<CB>& L,
+                                        float* sPart, int wg, int lane, int rg0, int rg1) {
   const int n = rg1 - rg0;
   const int ns = (n + RPG - 1) / RPG;
   auto rows_of = [&](int s) { return (n - s * RPG < RPG) ? n - s * RPG : RPG; };
   auto src_of = [&](int s) { return lane_src + uint32_t(rg0 + s * RPG) * row_bytes; };
-  for (int s = 0; s < ns; s += 3) {
+  for (int s = 0; s < ns; s += 2) {
     compute_step<CB, RPG, kFast>(A, L, sPart, p.spr, p.W, wg, lane, rg0 + s * RPG, rows_of(s));
-    if (s + 3 < ns) load_step<CB, RPG>(A, src_of(s + 3), row_bytes, rows_of(s + 3));
+    if (s + 2 < ns) load_step<CB, RPG>(A, src_of(s + 2), row_bytes, rows_of(s + 2));
     if (s + 1 < ns) {
       compute_step<CB, RPG, kFast>(B, L, sPart, p.spr, p.W, wg, lane, rg0 + (s + 1) * RPG,
                                    rows_of(s + 1));
-      if (s + 4 < ns) load_step<CB, RPG>(B, src_of(s + 4), row_bytes, rows_of(s + 4));
-    }
-    if (s + 2 < ns) {
-      compute_step<CB, RPG, kFast>(C, L, sPart, p.spr, p.W, wg, lane, rg0 + (s + 2) * RPG,
-                                   rows_of(s + 2));
-      if (s + 5 < ns) load_step<CB, RPG>(C, src_of(s + 5), row_bytes, rows_of(s + 5));
+      if (s + 3 < ns) load_step<CB, RPG>(B, src_of(s + 3), row_bytes, rows_of(s + 3));
     }
   }
 }
@@ -354,18 +349,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_b1_kernel(const B1Args p) {
       }
     }
   }
-  // The first three weight steps go out once this thread's small loads have
+  // The first two weight steps go out once this thread's small loads have
   // arrived and its x pieces are converted: loads queue per SM, so a small
   // load issued next to a weight stream would wait behind it.
   asm volatile("" ::: "memory");  // keep the weight loads after the stores above
-  Step<CB, RPG> A, B, C;
+  Step<CB, RPG> A, B;
   const int n_rows = rg1 - rg0;
   const int n_steps = (n_rows + RPG - 1) / RPG;
   auto rows_of = [&](int s) { return (n_rows - s * RPG < RPG) ? n_rows - s * RPG : RPG; };
   const uint32_t rb = uint32_t(row_bytes);
   if (n_steps > 0) load_step<CB, RPG>(A, lane_src + uint32_t(rg0) * rb, rb, rows_of(0));
   if (n_steps > 1) load_step<CB, RPG>(B, lane_src + uint32_t(rg0 + RPG) * rb, rb, rows_of(1));
-  if (n_steps > 2) load_step<CB, RPG>(C, lane_src + uint32_t(rg0 + 2 * RPG) * rb, rb, rows_of(2));
 
   // the table must be where the plan put it (64 KB-aligned) for the fast path
   const bool fast = !__syncthreads_or(!(x_exact && tab == smem + p.off_tab));
@@ -399,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_b1_kernel(const B1Args p) {
       L.x16[4 * q + 2] = v.z;
       L.x16[4 * q + 3] = v.w;
     }
-    consume<CB, RPG, true>(p, lane_src, uint32_t(row_bytes), A, B, C, L, sPart, wg, lane, rg0, rg1);
+    consume<CB, RPG, true>(p, lane_src, uint32_t(row_bytes), A, B, L, sPart, wg, lane, rg0, rg1);
   } else {
     L.xs = 1.0f;
 #pragma unroll
@@ -411,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_b1_kernel(const B1Args p) {
       for (int j = 0; j < 4; ++j)
         L.xf[4 * q + j] = make_float2(__uint_as_float(w[j] << 16), __uint_as_float(w[j] & 0xffff0000u));
     }
-    consume<CB, RPG, false>(p, lane_src, uint32_t(row_bytes), A, B, C, L, sPart, wg, lane, rg0, rg1);
+    consume<CB, RPG, false>(p, lane_src, uint32_t(row_bytes), A, B, L, sPart, wg, lane, rg0, rg1);
   }
 
   // End of the group: one sum per row over the group's warps, in order.
