@@ -49,6 +49,21 @@ def test_all_batches_and_chunk_widths(K, batch):
     assert_gemv_close(y, y_ref, s_abs, f"N={N} K={K} batch={batch}")
 
 
+@pytest.mark.parametrize("N,K", [(1536, 512), (4096, 4096), (37, 1536), (300, 8960), (1000, 40)])
+def test_batch1_binary32_x_fallback(N, K):
+    """x whose first 32-element chunk spans 2^60 .. 2^-60: no power-of-two
+    scaling of the chunk fits binary16, so every CTA of the batch-1 kernel
+    takes its binary32-x path (and K = 40 the generic kernel)."""
+    w = synth.weights(720 + K, N * K)
+    t = oracle.quantize(w, 64, 256, synth.code2_linear())
+    x = synth.activations(820 + K, 1, K).copy()
+    x[0, 0] = 0x5D80                                # bf16 2^60
+    x[0, 1] = 0x2180                                # bf16 2^-60
+    y = gpu_gemv(t, N, K, x)
+    y_ref, s_abs = oracle.gemv(t, N, K, x)
+    assert_gemv_close(y, y_ref, s_abs, f"N={N} K={K}")
+
+
 @pytest.mark.parametrize("N", [1, 2, 7, 31, 32, 33, 255, 256, 257, 1000])
 def test_row_counts(N):
     K = 1536

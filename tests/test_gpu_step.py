@@ -39,7 +39,7 @@ def _round_all(v: np.ndarray, dtype: int) -> np.ndarray:
     return np.vectorize(lambda a: oracle.round_f64(a, dtype), otypes=[np.uint32])(v)
 
 
-def _check_dag(spec, batch, seed, kernels=None):
+def _check_dag(spec, batch, seed, kernels=None, x_edit=None):
     """spec: list of (N, K, y dtype, has_bias, input) nodes. Builds the step
     from oracle-quantized weights, runs it once and checks every node's
     output against the oracle with the carried error bound:
@@ -61,6 +61,8 @@ def _check_dag(spec, batch, seed, kernels=None):
         y = torch.full((batch, N), float("nan"), dtype=_TDT[dt], device=dev())
         nodes.append(dict(weight=_weight(t, N, K), y=y, bias=bt, input=inp))
     x_bits = synth.activations(seed + 99, batch, spec[0][1])
+    if x_edit is not None:
+        x_bits = x_edit(x_bits.copy())
     x = u16_to_torch(x_bits, torch.bfloat16).view(batch, -1)
     step = nf4.DecodeStep(nodes, x)
     if kernels is not None:
@@ -160,6 +162,18 @@ def test_full_size_layers_group_qkv_and_gate_up(model):
         torch.cuda.synchronize()
         assert nf4.nf4_device_error_flags() == 0
         step.close()
+
+
+def test_step_with_binary32_x_input():
+    """The step's input spans 2^10 .. 2^-30 in its first 32-element chunk (a
+    range binary16 cannot hold after any power-of-two scaling), so the first
+    launch (q/k/v) runs the batch-1 kernel's binary32-x path inside the
+    recorded graph; the values stay inside the binary16 output range of v."""
+    def extreme(x):
+        x[:, 0] = 0x4480                            # bf16 2^10
+        x[:, 1] = 0x3080                            # bf16 2^-30
+        return x
+    _check_dag(_small_decoder(1), 1, 265, kernels=4, x_edit=extreme)
 
 
 def test_small_and_fallback_node_groups():
